@@ -1,0 +1,196 @@
+/*
+ * csa.h -- C ABI of libcsa.so: compressed sparse attention (CSA) decode on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * One CSA layer, one decode (or chunked-prefill) step, for T query tokens:
+ *
+ *   1. lightning indexer   I[t,s] = sum_h w[t,h] * ReLU(q^I[t,h] . K^I[s])
+ *      over the compressed blocks s visible to token t;
+ *   2. top-k               the top_k highest-scoring visible blocks;
+ *   3. mixed gather        their compressed rows, then the sliding-window rows;
+ *   4. shared-KV MQA       softmax attention of the H query heads over those
+ *                          rows, each 512-wide row serving as key and value.
+ *
+ * Sources (web pages of the nvfp4-megamoe-kernel project):
+ *   [Audit rewrite]  "ARCHITECTURE & MEMORY AUDIT -- Post-probe rewrite":
+ *                    F1 (128-wide indexer keys shared by the 64 indexer heads),
+ *                    F3 (the scoring formula, eq. 16 of the DSv4 paper
+ *                    section 2.3.1, and the einsum 'tnd,cd->tnc'), B2 (no silent
+ *                    fallback when the top-k is missing), C1 (capacity sized
+ *                    by ceil(context / ratio)), C2 (pre-allocated gather buffer).
+ *   [Audit 1M]       "ARCHITECTURE & MEMORY AUDIT -- 1M-context viability":
+ *                    D3 (gather of selected rows + window), D5 (window kept
+ *                    beside the compressed rows), D6 (attention sink),
+ *                    M2 (overflow of the compressed buffer), M5 (attention that
+ *                    reads rows by index with no gather buffer).
+ *   [Part A clues]   "PART A -- Next Session Clues", section 3 (a query sees
+ *                    only blocks strictly preceding its own; window and newest
+ *                    compressed block are both attended).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless marked (host).  All device buffers
+ *     are owned and allocated by the caller; the library never allocates,
+ *     frees or synchronises, and keeps no state between calls.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     only enqueued; results are ready when the stream reaches that point.
+ *   - Host-side argument errors return before anything is launched.
+ *   - Errors found by the kernels (an index out of range, a window row the
+ *     ring no longer holds, an inconsistent layout) are OR-ed into the
+ *     caller's device word `dev_status` (CSA_DEV_* bits; the caller zeroes it);
+ *     the offending row or token is skipped, nothing traps.
+ *   - bf16 is IEEE bfloat16 (uint16 storage); f32 is IEEE binary32.
+ *   - Every buffer is dense row-major with the shape given; every device
+ *     pointer must be 16-byte aligned.
+ */
+#ifndef CSA_H
+#define CSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CSA_ABI_VERSION 1
+
+typedef enum {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misaligned buffer */
+    CSA_ERR_UNSUPPORTED = 2,      /* dims or device this build does not handle */
+    CSA_ERR_CAPACITY = 3,         /* a buffer is smaller than the layout needs */
+    CSA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+    CSA_ERR_DEVICE_FAULT = 5,     /* reserved: a device-status bit was read back */
+    CSA_ERR_TIMEOUT = 6,          /* reserved: a bounded device wait gave up */
+    CSA_ERR_WORKSPACE = 7         /* workspace missing or smaller than csa_workspace_size */
+} csa_status_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define CSA_DEV_BAD_INDEX   0x01  /* idx outside [0, n_vis) for a selected slot */
+#define CSA_DEV_MISSING_SWA 0x02  /* a window position below swa_first_pos */
+#define CSA_DEV_BAD_LAYOUT  0x04  /* tok_seq outside [0,B), tok_pos < 0, bad comp_off */
+#define CSA_DEV_CAPACITY    0x08  /* a sequence holds more blocks than max_comp_rows */
+#define CSA_DEV_BAD_LENGTH  0x10  /* kv_len outside [0, top_k + window] */
+#define CSA_DEV_TIMEOUT     0x20  /* reserved for bounded waits */
+
+/* Where each query token's rows live.  Device arrays unless marked (host). */
+typedef struct {
+    int32_t num_seqs;               /* (host) B >= 1 */
+    int32_t num_tokens;             /* (host) T >= 0 */
+    int64_t total_comp_rows;        /* (host) R = comp_off[B], rows in k_idx / comp_kv */
+    int64_t max_comp_rows;          /* (host) upper bound of comp_off[b+1]-comp_off[b];
+                                       sizes grids and workspace without a device read */
+    const int32_t *tok_seq;         /* [T] sequence of each query token */
+    const int64_t *tok_pos;         /* [T] absolute 0-based position of each query token */
+    const int64_t *comp_off;        /* [B+1] block b of sequence s is row comp_off[s] + b */
+    const void *swa_kv;             /* bf16 [B, swa_cap, hd]: position p at slot p % swa_cap */
+    int32_t swa_cap;                /* (host) ring slots per sequence, >= window */
+    const int64_t *swa_first_pos;   /* [B] oldest position the ring still holds */
+} csa_layout_t;
+
+/* Problem constants.  This build supports n_ih = 64, ihd = 128, hd = 512,
+ * n_heads a multiple of 16 up to 128, 1 <= top_k <= 2048, window <= swa_cap. */
+typedef struct {
+    int32_t n_ih;     /* indexer heads (64) */
+    int32_t ihd;      /* indexer head dim = width of the shared block key (128) */
+    int32_t hd;       /* main head dim = width of a compressed / window row (512) */
+    int32_t n_heads;  /* main query heads H */
+    int32_t top_k;    /* selected blocks per token (1024) */
+    int32_t window;   /* sliding-window rows per token (128) */
+    int32_t ratio;    /* tokens per compressed block (4 for CSA) */
+    float scale;      /* attention logit scale (1/sqrt(hd)) */
+} csa_params_t;
+
+/* Derived rule used by every entry point ([Part A clues], section 3):
+ *   n_vis(t) = min(comp_off[b+1] - comp_off[b], floor(tok_pos[t] / ratio)),
+ *   b = tok_seq[t]: token t sees blocks 0 .. n_vis(t)-1 of its sequence.
+ * Window of token t: positions max(0, p - window + 1) .. p, p = tok_pos[t]. */
+
+/* Human-readable name of a status code (static storage). */
+const char *csa_status_string(csa_status_t status);
+
+/* CSA_ABI_VERSION of the loaded library. */
+int32_t csa_abi_version(void);
+
+/* Bytes of workspace `ws` that csa_topk, csa_sparse_mqa_decode and csa_decode
+ * need for this layout and these params (one size serves all three).
+ * The workspace must be zero-filled before its first use; each call that
+ * completes without error leaves it zero-filled again, so it can be reused
+ * by the next call on the same stream with no memset.  After a call that
+ * returned an error or set a dev_status bit, zero it again.  Calls that may
+ * run concurrently (different streams) need separate workspaces.
+ * Returns CSA_ERR_INVALID_ARGUMENT / CSA_ERR_UNSUPPORTED on bad input. */
+csa_status_t csa_workspace_size(const csa_layout_t *layout, const csa_params_t *params,
+                                size_t *bytes /* (host) out */);
+
+/* Step 1, the lightning indexer ([Audit rewrite], F1 and F3):
+ *   scores[t, s] = sum_h w_idx[t,h] * max(0, sum_d q_idx[t,h,d] * k_idx[comp_off[b]+s, d])
+ * for s < n_vis(t); entries s >= n_vis(t) are not written.
+ *   q_idx  bf16 [T, n_ih, ihd]     w_idx f32 [T, n_ih]
+ *   k_idx  bf16 [R, ihd]           scores f32 [T, ld_scores], ld_scores >= max_comp_rows,
+ *                                  ld_scores a multiple of 4.
+ * Products are exact (bf16 x bf16), sums are f32 (tensor-core accumulation
+ * over d, then a fixed-order sum over h).  The result does not depend on the
+ * stream, launch order or other tokens. */
+csa_status_t csa_indexer_scores(const csa_layout_t *layout, const csa_params_t *params,
+                                const void *q_idx, const float *w_idx, const void *k_idx,
+                                float *scores, int64_t ld_scores, int32_t *dev_status,
+                                void *stream);
+
+/* Step 2, top-k over the visible scores ([Audit rewrite], F3: total.topk):
+ * keeps k'(t) = min(top_k, n_vis(t)) blocks ranked by (score descending,
+ * block index ascending; -0.0 ties with +0.0), writes them to idx[t, 0..k')
+ * in ascending block index and -1 in idx[t, k'..top_k); n_sel[t] = k'.
+ *   scores f32 [T, ld_scores] (as written by csa_indexer_scores; NaN unsupported)
+ *   idx    int32 [T, top_k]      n_sel int32 [T]
+ * Exact: the selection is a pure function of the scores' bits. */
+csa_status_t csa_topk(const csa_layout_t *layout, const csa_params_t *params,
+                      const float *scores, int64_t ld_scores, int32_t *idx, int32_t *n_sel,
+                      int32_t *dev_status, void *ws, size_t ws_bytes, void *stream);
+
+/* Step 3, mixed gather into a caller-owned buffer ([Audit 1M], D3 and D5;
+ * [Audit rewrite], C2):
+ *   kv_buf[t, i]          = comp_kv[comp_off[b] + idx[t, i]],  i < n_sel[t]
+ *   kv_buf[t, n_sel + j]  = swa_kv[b, x_j % swa_cap],  x_j = first + j, oldest first
+ *   kv_len[t]             = n_sel[t] + (p - first + 1)
+ * Both the compressed rows and the window rows are kept even where they cover
+ * the same tokens.  Rows kv_buf[t, kv_len[t] ..) are left untouched.
+ *   idx int32 [T, top_k], n_sel int32 [T], comp_kv bf16 [R, hd],
+ *   kv_buf bf16 [T, top_k + window, hd], kv_len int32 [T].
+ * An idx outside [0, n_vis(t)) sets CSA_DEV_BAD_INDEX and that row is
+ * written as zeros (no clamping); a window position the ring no longer holds
+ * sets CSA_DEV_MISSING_SWA and that row is written as zeros. */
+csa_status_t csa_gather_mixed(const csa_layout_t *layout, const csa_params_t *params,
+                              const int32_t *idx, const int32_t *n_sel, const void *comp_kv,
+                              void *kv_buf, int32_t *kv_len, int32_t *dev_status,
+                              void *stream);
+
+/* Step 4, shared-KV multi-query attention over gathered rows ([Audit 1M], D5):
+ *   l_j = scale * q[t,h,:] . kv_buf[t,j,:],  j < kv_len[t]
+ *   out[t,h,:] = sum_j softmax_j(l) * kv_buf[t,j,:]
+ * With sinks != NULL (f32 [H]), exp(sinks[h] - max) joins the softmax
+ * denominator of head h ([Audit 1M], D6); NULL means no sink.
+ *   q bf16 [T, H, hd], kv_buf bf16 [T, top_k + window, hd], kv_len int32 [T],
+ *   out f32 [T, H, hd].  kv_len[t] = 0 gives out[t] = 0.
+ * bf16 x bf16 products on tensor cores, f32 accumulation and softmax. */
+csa_status_t csa_sparse_mqa_decode(int32_t num_tokens, const csa_params_t *params,
+                                   const void *q, const void *kv_buf, const int32_t *kv_len,
+                                   const float *sinks, float *out, int32_t *dev_status,
+                                   void *ws, size_t ws_bytes, void *stream);
+
+/* Steps 1-4 fused ([Audit 1M], M5): the indexer feeds the top-k through the
+ * workspace, and attention reads the selected compressed rows by index
+ * straight from comp_kv and the window rows straight from the ring; no
+ * gather buffer exists.  Same inputs and outputs as the four calls above;
+ * idx_out (nullable, int32 [T, top_k]) receives the selection exactly as
+ * csa_topk would write it for the scores csa_indexer_scores computes. */
+csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params,
+                        const void *q_idx, const float *w_idx, const void *k_idx,
+                        const void *comp_kv, const void *q, const float *sinks, float *out,
+                        int32_t *idx_out, int32_t *dev_status, void *ws, size_t ws_bytes,
+                        void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H */

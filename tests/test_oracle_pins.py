@@ -1,0 +1,407 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, independent of the oracle's own code.
+
+Each group names the failure it is there to catch (a dropped ReLU, a wrong
+sign, a transposed operand, the per-head key algebra, an off-by-one in the
+causal rule, a wrong tie-break, a wrong window order ...).
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import csa_workloads as W
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(a) -> np.ndarray:
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- visibility
+
+def test_visibility_golden_table():
+    rows = read_golden("visibility_cases.txt")
+    assert len(rows) >= 15
+    for pos, n_comp, ratio, expect in rows:
+        assert oracle.n_vis(int(n_comp), int(pos), int(ratio)) == int(expect), (pos, n_comp)
+
+
+def test_visibility_brute_force_block_membership():
+    # Block j = positions [r*j, r*j + r); visible iff every position of block j
+    # is < pos (strictly preceding) and j < n_comp.  Enumerate positions.
+    for ratio in (1, 2, 4, 8):
+        for n_comp in range(0, 7):
+            for pos in range(0, 40):
+                vis = sum(1 for j in range(n_comp)
+                          if all(x < pos for x in range(ratio * j, ratio * j + ratio))
+                          and not (ratio * j <= pos < ratio * j + ratio))
+                assert oracle.n_vis(n_comp, pos, ratio) == vis
+
+
+# ------------------------------------------------------------------- indexer
+
+def _closed_form_case(n_ih=64, ihd=128, n_blocks=300):
+    # q[h, d] = (h+1) * (-1)^d, k_s = e_{s mod ihd}  =>  q_h . k_s = (h+1)(-1)^s
+    q = np.array([[(h + 1) * (-1) ** d for d in range(ihd)] for h in range(n_ih)], np.float32)
+    k = np.zeros((n_blocks, ihd), np.float32)
+    for s in range(n_blocks):
+        k[s, s % ihd] = 1.0
+    return bf16_bits(q), bf16_bits(k)
+
+
+def test_indexer_closed_form_alternating_sign():
+    """w = 1: score = sum_h ReLU((h+1)(-1)^s) = 2080 (even s) and 0 (odd s).
+    A dropped ReLU gives -2080 on odd blocks; a dropped head gives < 2080."""
+    qb, kb = _closed_form_case()
+    n_blocks = kb.shape[0]
+    w = np.ones((1, 64), np.float32)
+    sc, nv = oracle.indexer_scores(qb[None], w, kb, [0], [4 * n_blocks], [0, n_blocks])
+    assert nv[0] == n_blocks
+    expect = np.array([2080.0 if (s % 128) % 2 == 0 else 0.0 for s in range(n_blocks)])
+    np.testing.assert_array_equal(sc[0, :n_blocks], expect)
+
+
+def test_indexer_closed_form_signed_weights():
+    """w_h = (-1)^h: even s -> sum_h (-1)^h (h+1) = -32 exactly; odd s -> 0."""
+    qb, kb = _closed_form_case(n_blocks=8)
+    w = np.array([[(-1.0) ** h for h in range(64)]], np.float32)
+    sc, _ = oracle.indexer_scores(qb[None], w, kb, [0], [32], [0, 8])
+    np.testing.assert_array_equal(sc[0, :8], [-32.0, 0.0] * 4)
+
+
+def test_indexer_closed_form_triangular():
+    """q_h = first h+1 ones, k_s = first s+1 ones => q_h . k_s = min(h, s) + 1.
+    Transposing q (d <-> h) or summing over the wrong axis breaks this."""
+    n_ih, ihd, n = 64, 128, 128
+    q = np.zeros((n_ih, ihd), np.float32)
+    for h in range(n_ih):
+        q[h, : h + 1] = 1.0
+    k = np.zeros((n, ihd), np.float32)
+    for s in range(n):
+        k[s, : s + 1] = 1.0
+    w = (np.arange(n_ih, dtype=np.float32) + 1.0)[None] / 64.0   # exact in bf16/f32
+    sc, _ = oracle.indexer_scores(bf16_bits(q)[None], w, bf16_bits(k), [0], [4 * n], [0, n])
+    expect = [sum((h + 1) / 64.0 * (min(h, s) + 1) for h in range(n_ih)) for s in range(n)]
+    np.testing.assert_allclose(sc[0, :n], expect, rtol=0, atol=1e-12)
+
+
+def test_indexer_one_hot_weights_is_relu_gemv():
+    """w = e_h reduces the score to ReLU(K q_h): a plain matrix-vector product."""
+    wl = W.make(seed=3, seq_lens=[4 * 200], n_comp=[200], n_heads=4)
+    qb = W.bits(wl.q_idx)
+    kb = W.bits(wl.k_idx)
+    K = bits_to_f64(kb)
+    for h in (0, 17, 63):
+        w = np.zeros((1, 64), np.float32)
+        w[0, h] = 1.0
+        sc, nv = oracle.indexer_scores(qb, w, kb, [0], [800], [0, 200])
+        ref = np.maximum(K @ bits_to_f64(qb[0, h]), 0.0)
+        np.testing.assert_allclose(sc[0, :200], ref, rtol=1e-13, atol=1e-12)
+
+
+def test_indexer_nonnegative_terms_and_homogeneity():
+    wl = W.make(seed=4, seq_lens=[4 * 256], n_comp=[256], n_heads=4)
+    qb, kb = W.bits(wl.q_idx), W.bits(wl.k_idx)
+    w = np.abs(wl.w_idx.numpy())
+    sc, _ = oracle.indexer_scores(qb, w, kb, [0], [1024], [0, 256])
+    assert (sc[0, :256] >= 0).all() and (sc[0, :256] > 0).any()
+    sc2, _ = oracle.indexer_scores(qb, 2.0 * wl.w_idx.numpy(), kb, [0], [1024], [0, 256])
+    sc1, _ = oracle.indexer_scores(qb, wl.w_idx.numpy(), kb, [0], [1024], [0, 256])
+    np.testing.assert_array_equal(sc2[0, :256], 2.0 * sc1[0, :256])
+
+
+def test_indexer_mqa_einsum_cross_check():
+    """The pages' corrected einsum 'tnd,cd->tnc' -> ReLU -> x w -> sum over heads,
+    evaluated with numpy in float64 on a multi-token, multi-sequence layout."""
+    wl = W.make(seed=5, seq_lens=[40, 100], tokens=[3, 2], n_comp=[10, 25], n_heads=2)
+    qb, kb = W.bits(wl.q_idx), W.bits(wl.k_idx)
+    sc, nv = oracle.indexer_scores(qb, wl.w_idx.numpy(), kb, wl.tok_seq.numpy(),
+                                   wl.tok_pos.numpy(), wl.comp_off.numpy())
+    Q, K, Wt = bits_to_f64(qb), bits_to_f64(kb), wl.w_idx.numpy().astype(np.float64)
+    for t in range(wl.num_tokens):
+        b = int(wl.tok_seq[t])
+        off = int(wl.comp_off[b])
+        n = int(nv[t])
+        assert n == min(int(wl.comp_off[b + 1]) - off, int(wl.tok_pos[t]) // 4)
+        raw = np.einsum("nd,cd->nc", Q[t], K[off:off + n])
+        ref = (np.maximum(raw, 0.0) * Wt[t][:, None]).sum(0)
+        np.testing.assert_allclose(sc[t, :n], ref, rtol=1e-12, atol=1e-10)
+
+
+def test_per_head_key_algebra_is_rejected():
+    """Negative control (Post-probe rewrite, F3): widening the 128-wide key
+    buffer to n_ih*ihd and giving every head its own slice changes the scores.
+    The closed-form pin above would catch an oracle that did this."""
+    qb, kb = _closed_form_case(n_blocks=4)
+    q = bits_to_f64(qb)
+    k = bits_to_f64(kb)
+    wide = np.zeros((4, 64, 128))
+    wide[:, 0, :] = k              # the real key lands in head 0's slice only
+    wrong = np.einsum("nd,cnd->nc", q, wide)
+    wrong = np.maximum(wrong, 0).sum(0)
+    sc, _ = oracle.indexer_scores(qb[None], np.ones((1, 64), np.float32), kb, [0], [16], [0, 4])
+    assert not np.allclose(wrong, sc[0, :4])
+    np.testing.assert_array_equal(sc[0, :4], [2080.0, 0.0, 2080.0, 0.0])
+
+
+# --------------------------------------------------------------------- top-k
+
+def _dominance_subsets(scores, k):
+    """Every k-subset S with: for i in S, j not in S, i ranks before j under
+    (score desc, index asc).  Exactly one exists."""
+    n = len(scores)
+    out = []
+    for S in itertools.combinations(range(n), k):
+        rest = [j for j in range(n) if j not in S]
+        if all(scores[i] > scores[j] or (scores[i] == scores[j] and i < j)
+               for i in S for j in rest):
+            out.append(list(S))
+    return out
+
+
+def test_topk_brute_force_tiny_with_ties():
+    rng = np.random.default_rng(0)
+    for trial in range(300):
+        n = int(rng.integers(0, 11))
+        k = int(rng.integers(1, 6))
+        scores = rng.integers(-3, 4, size=n).astype(np.float64)   # many ties
+        idx, n_sel = oracle.topk(scores, k)
+        kk = min(k, n)
+        subs = _dominance_subsets(list(scores), kk)
+        assert len(subs) == 1, (scores, k)
+        assert n_sel == kk
+        assert list(idx[:kk]) == subs[0]
+        assert (idx[kk:] == -1).all()
+
+
+def test_topk_matches_lexsort():
+    """A library routine: numpy lexsort on (index, -score)."""
+    rng = np.random.default_rng(1)
+    for n, k in [(1000, 64), (5000, 1024), (300, 300), (17, 1024)]:
+        scores = np.round(rng.normal(size=n), 2)
+        idx, n_sel = oracle.topk(scores, k)
+        order = np.lexsort((np.arange(n), -scores))[: min(k, n)]
+        assert n_sel == min(k, n)
+        np.testing.assert_array_equal(idx[:n_sel], np.sort(order))
+
+
+def test_topk_signed_zero_ties_and_padding():
+    scores = np.array([0.0, -0.0, 0.0, -1.0, -0.0])
+    idx, n_sel = oracle.topk(scores, 2)
+    assert n_sel == 2 and list(idx) == [0, 1]
+    idx, n_sel = oracle.topk(np.array([5.0, -0.0, 0.0]), 2)
+    assert list(idx) == [0, 1]
+    idx, n_sel = oracle.topk(np.zeros(0), 4)
+    assert n_sel == 0 and list(idx) == [-1] * 4
+    idx, n_sel = oracle.topk(np.array([1.0, 3.0, 2.0]), 8)
+    assert n_sel == 3 and list(idx) == [0, 1, 2] + [-1] * 5
+
+
+def test_topk_rejects_nan():
+    with pytest.raises(oracle.OracleError):
+        oracle.topk(np.array([1.0, np.nan]), 1)
+
+
+# -------------------------------------------------------------------- gather
+
+def test_gather_rows_and_window_order():
+    wl = W.make(seed=6, seq_lens=[50, 300], tokens=[1, 2], n_comp=[12, 75], top_k=8,
+                window=16, swa_cap=32, hd=8, n_heads=2)
+    idx = np.full((3, 8), -1, np.int32)
+    n_sel = np.array([3, 8, 0], np.int32)
+    idx[0, :3] = [0, 5, 11]
+    idx[1, :8] = [1, 2, 3, 10, 20, 40, 74, 0]
+    comp_kv, swa = W.bits(wl.comp_kv), W.bits(wl.swa_kv)
+    buf, kv_len = oracle.gather(idx, n_sel, comp_kv, swa, wl.tok_seq.numpy(),
+                                wl.tok_pos.numpy(), wl.comp_off.numpy(),
+                                wl.swa_first_pos.numpy(), top_k=8, window=16)
+    assert list(kv_len) == [3 + 16, 8 + 16, 0 + 16]
+    for t in range(3):
+        b = int(wl.tok_seq[t])
+        p = int(wl.tok_pos[t])
+        off = int(wl.comp_off[b])
+        for i in range(n_sel[t]):
+            np.testing.assert_array_equal(buf[t, i], comp_kv[off + idx[t, i]])
+        for j, x in enumerate(range(p - 15, p + 1)):          # oldest -> newest
+            np.testing.assert_array_equal(buf[t, n_sel[t] + j], swa[b, x % 32])
+
+
+def test_gather_short_sequence_window_and_errors():
+    wl = W.make(seed=7, seq_lens=[5], tokens=[1], n_comp=[1], top_k=4, window=16, hd=8,
+                n_heads=1)
+    buf, kv_len = oracle.gather(np.array([[0, -1, -1, -1]]), np.array([1]), W.bits(wl.comp_kv),
+                                W.bits(wl.swa_kv), [0], [5], [0, 1], [0], top_k=4, window=16)
+    assert kv_len[0] == 1 + 6           # positions 0..5
+    with pytest.raises(oracle.OracleError) as e:      # block 1 is not visible at pos 5
+        oracle.gather(np.array([[1, -1, -1, -1]]), np.array([1]), W.bits(wl.comp_kv),
+                      W.bits(wl.swa_kv), [0], [5], [0, 2], [0], top_k=4, window=16)
+    assert e.value.code == oracle.EINDEX
+    with pytest.raises(oracle.OracleError) as e:      # ring no longer holds position 0
+        oracle.gather(np.array([[0, -1, -1, -1]]), np.array([1]), W.bits(wl.comp_kv),
+                      W.bits(wl.swa_kv), [0], [5], [0, 1], [1], top_k=4, window=16)
+    assert e.value.code == oracle.ESWA
+
+
+# ----------------------------------------------------------------- attention
+
+def _sdpa_f64(q_bits, rows_bits, scale):
+    q = torch.from_numpy(bits_to_f64(q_bits))[None]            # [1, H, hd]
+    kv = torch.from_numpy(bits_to_f64(rows_bits))[None, None]  # [1, 1, L, hd]
+    kv = kv.expand(1, q.shape[1], -1, -1)
+    o = torch.nn.functional.scaled_dot_product_attention(q[:, :, None, :].transpose(0, 0), kv,
+                                                         kv, scale=scale)
+    return o[0, :, 0, :].numpy()
+
+
+def test_attention_matches_sdpa_f64():
+    rng = np.random.default_rng(8)
+    H, hd, L = 4, 64, 37
+    q = bf16_bits(rng.normal(size=(1, H, hd)))
+    rows = bf16_bits(rng.normal(size=(1, 50, hd)))
+    out = oracle.attention(q, rows, [L], scale=1 / math.sqrt(hd))
+    q4 = torch.from_numpy(bits_to_f64(q))[:, :, None, :]             # [1, H, 1, hd]
+    kv = torch.from_numpy(bits_to_f64(rows[:, :L]))[:, None].expand(1, H, L, hd)
+    ref = torch.nn.functional.scaled_dot_product_attention(q4, kv, kv, scale=1 / math.sqrt(hd))
+    np.testing.assert_allclose(out[0], ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(9)
+    H, hd = 3, 32
+    q = bf16_bits(rng.normal(size=(1, H, hd)))
+    rows = bf16_bits(rng.normal(size=(1, 20, hd)))
+    # a single row returns that row exactly
+    out = oracle.attention(q, rows, [1], scale=0.3)
+    for h in range(H):
+        np.testing.assert_array_equal(out[0, h], bits_to_f64(rows[0, 0]))
+    # identical rows return that row
+    same = np.repeat(rows[:, :1], 20, axis=1)
+    out = oracle.attention(q, same, [20], scale=0.3)
+    np.testing.assert_allclose(out[0], np.repeat(bits_to_f64(rows[0, :1]), H, 0), rtol=1e-14)
+    # q = 0 gives the mean of the rows
+    out = oracle.attention(np.zeros_like(q), rows, [20], scale=0.3)
+    np.testing.assert_allclose(out[0, 1], bits_to_f64(rows[0]).mean(0), rtol=1e-13, atol=1e-15)
+    # permuting the rows changes nothing beyond rounding
+    perm = rng.permutation(20)
+    a = oracle.attention(q, rows, [20], scale=0.3)
+    b = oracle.attention(q, rows[:, perm], [20], scale=0.3)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-14)
+    # outputs are convex combinations of the rows
+    r = bits_to_f64(rows[0])
+    assert (a[0] <= r.max(0) + 1e-12).all() and (a[0] >= r.min(0) - 1e-12).all()
+
+
+def test_attention_sink_identity():
+    """With a sink logit s_h: out_sink = out * sigmoid(logsumexp(l) - s_h)."""
+    rng = np.random.default_rng(10)
+    H, hd, L = 4, 16, 9
+    q = bf16_bits(rng.normal(size=(1, H, hd)))
+    rows = bf16_bits(rng.normal(size=(1, L, hd)))
+    sinks = rng.normal(size=H).astype(np.float32) * 2
+    base = oracle.attention(q, rows, [L], scale=0.25)
+    withs = oracle.attention(q, rows, [L], scale=0.25, sinks=sinks)
+    logits = torch.from_numpy(0.25 * bits_to_f64(q[0]) @ bits_to_f64(rows[0]).T)
+    lse = torch.logsumexp(logits, dim=1).numpy()
+    factor = 1.0 / (1.0 + np.exp(sinks.astype(np.float64) - lse))
+    np.testing.assert_allclose(withs[0], base[0] * factor[:, None], rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------------- the whole step
+
+def _visible_rows(wl, t, nv):
+    b = int(wl.tok_seq[t])
+    p = int(wl.tok_pos[t])
+    off = int(wl.comp_off[b])
+    comp = W.bits(wl.comp_kv)[off:off + nv]
+    first = max(0, p - wl.window + 1)
+    swa = np.stack([W.bits(wl.swa_kv)[b, x % wl.swa_cap] for x in range(first, p + 1)])
+    return np.concatenate([comp, swa])
+
+
+def test_decode_reduces_to_dense_attention_when_topk_covers_all():
+    wl = W.make(seed=11, seq_lens=[4 * 30 + 2, 70], tokens=[2, 1], n_comp=[30, 17],
+                top_k=64, window=16, swa_cap=20, hd=64, n_heads=4)
+    idx, n_sel, out = oracle.decode(W.bits(wl.q_idx), wl.w_idx.numpy(), W.bits(wl.k_idx),
+                                    W.bits(wl.comp_kv), W.bits(wl.swa_kv), W.bits(wl.q),
+                                    wl.tok_seq.numpy(), wl.tok_pos.numpy(), wl.comp_off.numpy(),
+                                    wl.swa_first_pos.numpy(), top_k=64, window=16)
+    for t in range(wl.num_tokens):
+        b = int(wl.tok_seq[t])
+        nv = min(int(wl.comp_off[b + 1] - wl.comp_off[b]), int(wl.tok_pos[t]) // 4)
+        assert n_sel[t] == nv
+        assert list(idx[t, :nv]) == list(range(nv))
+        rows = _visible_rows(wl, t, nv)
+        q4 = torch.from_numpy(bits_to_f64(W.bits(wl.q)[t]))[None, :, None, :]
+        kv = torch.from_numpy(bits_to_f64(rows))[None, None].expand(1, 4, -1, -1)
+        ref = torch.nn.functional.scaled_dot_product_attention(q4, kv, kv, scale=wl.scale)
+        np.testing.assert_allclose(out[t], ref[0, :, 0].numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_decode_causality_perturbation():
+    """Changing any block at or after n_vis, or any ring slot outside the
+    window, leaves the selection and the output bit-identical."""
+    wl = W.make(seed=12, seq_lens=[4 * 40 + 1], tokens=[1], n_comp=[40], comp_capacity=[48],
+                top_k=8, window=8, swa_cap=16, hd=32, n_heads=2)
+    args = lambda w: (W.bits(w.q_idx), w.w_idx.numpy(), W.bits(w.k_idx), W.bits(w.comp_kv),
+                      W.bits(w.swa_kv), W.bits(w.q), w.tok_seq.numpy(), w.tok_pos.numpy(),
+                      w.comp_off.numpy(), w.swa_first_pos.numpy())
+    idx0, ns0, out0 = oracle.decode(*args(wl), top_k=8, window=8)
+    nv = 40
+    g = torch.Generator().manual_seed(99)
+    wl.k_idx[nv:] = W.bf16_normal(g, 8, wl.ihd) * 50
+    wl.comp_kv[nv:] = W.bf16_normal(g, 8, wl.hd) * 50
+    p = int(wl.tok_pos[0])
+    inside = {x % 16 for x in range(p - 7, p + 1)}
+    for slot in range(16):
+        if slot not in inside:
+            wl.swa_kv[0, slot] = W.bf16_normal(g, wl.hd) * 50
+    # grow the packed offsets: the extra rows exist but are not visible at p
+    wl.comp_off[1] = 48
+    idx1, ns1, out1 = oracle.decode(*args(wl), top_k=8, window=8)
+    np.testing.assert_array_equal(idx0, idx1)
+    np.testing.assert_array_equal(out0, out1)
+    assert (idx0[0, : ns0[0]] < nv).all()
+
+
+def test_planted_blocks_are_selected():
+    wl = W.make(seed=13, seq_lens=[4 * 4096], n_comp=[4096], top_k=128, n_heads=2, hd=32,
+                window=4, swa_cap=8)
+    W.plant_blocks(wl, 32, 4.0, seed=2)
+    sc, nv = oracle.indexer_scores(W.bits(wl.q_idx), wl.w_idx.numpy(), W.bits(wl.k_idx),
+                                   [0], wl.tok_pos.numpy(), wl.comp_off.numpy())
+    idx, n_sel = oracle.topk(sc[0, : nv[0]], 128)
+    assert set(wl.planted.tolist()) <= set(idx[:n_sel].tolist())
+
+
+# --------------------------------------------------------------------- sizes
+
+def test_memory_sizing_matches_pages():
+    g = {k: int(v) for k, v in read_golden("memory_sizing.txt")}
+    t = W.tiny()
+    assert t.k_idx[0].nbytes == g["indexer_key_bytes_per_block"]
+    assert t.comp_kv[0].nbytes == g["main_row_bytes_per_block"]
+    assert t.swa_kv[0].nbytes == g["swa_ring_bytes_per_layer"]
+    n1m = 262144
+    assert n1m * W.IHD * 2 == g["indexer_key_bytes_1m"]
+    assert n1m * W.HD * 2 == g["main_row_bytes_1m"]
