@@ -1,0 +1,470 @@
+"""Benchmark: CSA decode tokens/s per layer at 1M context on GB300.
+
+One step = one csa_decode (indexer -> top-k -> sparse shared-KV attention) for
+one query token over one CSA layer holding 262,144 compressed blocks (64 MiB
+of indexer keys, 256 MiB of 512-wide rows), top_k 1024, a 128-row window and
+64 query heads.  Steps rotate over independent layer copies whose caches
+total several times the 129 MB L2, so every step streams its keys from HBM.
+Each step is a CUDA-graph replay of the library's launches.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on the
+same workload instead (the only other place this file runs the oracle).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import csa_workloads as W  # noqa: E402
+
+METRIC = "CSA decode tokens/s per layer at 1M ctx (batch 1 & 32); % of HBM/tensor roofline"
+UNIT = "tokens/s/layer"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class Layer:
+    """One CSA layer's cache + one decode token's activations, on the GPU."""
+
+    def __init__(self, wl: W.Workload, device, csa):
+        d = wl.to(device)
+        self.wl, self.d = wl, d
+        self.layout = csa.Layout(d.tok_seq, d.tok_pos, d.comp_off, d.swa_kv, d.swa_first_pos,
+                                 max_comp_rows=wl.max_comp_rows,
+                                 total_comp_rows=int(wl.k_idx.shape[0]), swa_cap=wl.swa_cap)
+        self.prm = csa.params(wl.n_heads, wl.top_k, wl.window, wl.ratio, wl.scale)
+        T = wl.num_tokens
+        self.out = torch.empty(T, wl.n_heads, wl.hd, dtype=torch.float32, device=device)
+        self.idx = torch.empty(T, wl.top_k, dtype=torch.int32, device=device)
+
+
+def algorithmic_bytes(wl: W.Workload):
+    """Bytes the method must move for one step (measurement)."""
+    keys = rows = 0
+    T = wl.num_tokens
+    for t in range(T):
+        b = int(wl.tok_seq[t])
+        n_comp = int(wl.comp_off[b + 1] - wl.comp_off[b])
+        p = int(wl.tok_pos[t])
+        nv = min(n_comp, p // wl.ratio)
+        keys += nv * wl.ihd * 2
+        rows += (min(wl.top_k, nv) + min(wl.window, p + 1)) * wl.hd * 2
+    act = T * (wl.n_ih * wl.ihd * 2 + wl.n_ih * 4 + wl.n_heads * wl.hd * 2)
+    out = T * wl.n_heads * wl.hd * 4
+    return {"indexer": keys + T * (wl.n_ih * wl.ihd * 2 + wl.n_ih * 4),
+            "step": keys + rows + act + out, "keys": keys, "rows": rows}
+
+
+def make_layers(name: str, n_layers: int, device, csa, seed0: int):
+    gen_fn = {"1m": W.ctx1m, "batch32": W.batch32}[name]
+    return [Layer(gen_fn(seed=seed0 + i, device=device), device, csa) for i in range(n_layers)]
+
+
+def launches_in_graph(graph) -> int:
+    """Kernel nodes in a captured CUDA graph (through the driver API)."""
+    import ctypes
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+        h = ctypes.c_void_p(graph.raw_cuda_graph())
+        n = ctypes.c_size_t(0)
+        if cu.cuGraphGetNodes(h, None, ctypes.byref(n)) != 0:
+            return -1
+        nodes = (ctypes.c_void_p * n.value)()
+        cu.cuGraphGetNodes(h, nodes, ctypes.byref(n))
+        kinds = ctypes.c_int(0)
+        k = 0
+        for i in range(n.value):
+            cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(kinds))
+            k += 1 if kinds.value == 0 else 0    # CU_GRAPH_NODE_TYPE_KERNEL
+        return k
+    except (OSError, AttributeError):
+        return -1
+
+
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time: every rank's steps must finish inside it."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_graphs(graphs, steps, warmup, stream):
+    for i in range(warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        graphs[(warmup + i) % len(graphs)].replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
+def run_ours(args, rank, world, device):
+    from sparse_compressed_kv_gb300 import csa
+    from sparse_compressed_kv_gb300 import build as cuda_build
+    cuda_build.build()
+    csa.load()
+    hbm_peak, tf_peak, peak_kind = peaks()
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device=device)
+
+    layers = make_layers("1m", args.layers, device, csa, seed0=1000 * rank)
+    wl0 = layers[0].wl
+    ab = algorithmic_bytes(wl0)
+    ws = csa.workspace(layers[0].layout, layers[0].prm)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def step(L, s):
+        csa.csa_decode(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, L.d.comp_kv, L.d.q,
+                       L.out, status, ws, idx_out=L.idx, stream=s)
+
+    # eager warm-up outside capture (sets kernel attributes, caches device info)
+    with torch.cuda.stream(stream):
+        for L in layers:
+            step(L, stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for L in layers:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(L, stream)
+        graphs.append(g)
+    per_step_launches = launches_in_graph(graphs[0])
+
+    # ---- timed region: exactly `steps` decode steps
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    ms = time_graphs(graphs, args.steps, args.warmup, stream)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms, device)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x} during the timed region")
+    assert torch.isfinite(layers[0].out).all()
+
+    # ---- the dominant kernel alone (indexer), same rotating layers, CUDA events
+    sc_buf = torch.empty(1, wl0.max_comp_rows, dtype=torch.float32, device=device)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            L = layers[i % len(layers)]
+            csa.csa_indexer_scores(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, sc_buf,
+                                   status, stream=stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            L = layers[i % len(layers)]
+            csa.csa_indexer_scores(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, sc_buf,
+                                   status, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    idx_ms = e0.elapsed_time(e1) / args.steps
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        L = layers[0]
+        hq_idx = L.d.q_idx.cpu().pin_memory()
+        hw_idx = L.d.w_idx.cpu().pin_memory()
+        hq = L.d.q.cpu().pin_memory()
+        hout = torch.empty(L.out.shape, dtype=torch.float32).pin_memory()
+        n_e2e = max(3, args.steps)
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + n_e2e):
+                if i == args.warmup:
+                    torch.cuda.synchronize()
+                    t_start = time.perf_counter()
+                L = layers[i % len(layers)]
+                L.d.q_idx.copy_(hq_idx, non_blocking=True)
+                L.d.w_idx.copy_(hw_idx, non_blocking=True)
+                L.d.q.copy_(hq, non_blocking=True)
+                step(L, stream)
+                hout.copy_(L.out, non_blocking=True)
+                stream.synchronize()
+        e2e_ms = (time.perf_counter() - t_start) * 1e3 / n_e2e
+        h2d = hq_idx.numel() * 2 + hw_idx.numel() * 4 + hq.numel() * 2
+        e2e = {"value": round(world * 1e3 / e2e_ms, 1), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 4)}
+
+    # ---- secondary: batched decode, 32 ragged sequences (32K..128K)
+    batch = None
+    if not args.no_batch32:
+        del graphs
+        blayers = make_layers("batch32", 2, device, csa, seed0=77 + 1000 * rank)
+        bws = csa.workspace(blayers[0].layout, blayers[0].prm)
+        bgraphs = []
+
+        def bstep(L, s):
+            csa.csa_decode(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, L.d.comp_kv, L.d.q,
+                           L.out, status, bws, idx_out=L.idx, stream=s)
+        with torch.cuda.stream(stream):
+            for L in blayers:
+                bstep(L, stream)
+        torch.cuda.synchronize()
+        for L in blayers:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                bstep(L, stream)
+            bgraphs.append(g)
+        bms = time_graphs(bgraphs, args.steps, args.warmup, stream)
+        bab = sum(algorithmic_bytes(L.wl)["step"] for L in blayers) / len(blayers)
+        batch = {"workload": "batch32: 32 sequences, contexts U{32K..128K}, one token each",
+                 "tokens_per_s_per_layer": round(32 * 1e3 / bms, 1), "ms_per_step": round(bms, 5),
+                 "algorithmic_bytes_per_step": int(bab),
+                 "hbm_frac": round(bab / (bms * 1e-3) / 1e9 / hbm_peak, 4)}
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("device status set in the batch32 region")
+
+    tok_s = world * 1e3 / ms
+    achieved = ab["indexer"] / (idx_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(tok_s, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "1m: CSA decode, 1 token, 262144 blocks (64 MiB keys, 256 MiB "
+                               "rows), top_k 1024, window 128, 64 heads, hd 512, 32 planted",
+                   "layers_rotated": args.layers,
+                   "l2": f"inputs > L2: {args.layers} independent layer caches "
+                         f"({args.layers * 0.34:.1f} GB) rotated, no flush",
+                   "parallelism": f"replicas x{world}", "graph": "one CUDA graph per step"},
+        "roofline": {"bound": "hbm", "kernel": "indexer (tcgen05, TMA)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "peak_kind": peak_kind, "kernel_ms": round(idx_ms, 5),
+                     "bytes_per_launch": ab["indexer"]},
+        "step_roofline": {"bound": "hbm", "algorithmic_bytes": ab["step"],
+                          "achieved": round(ab["step"] / (ms * 1e-3) / 1e9, 1),
+                          "peak": hbm_peak, "unit": "GB/s",
+                          "frac": round(ab["step"] / (ms * 1e-3) / 1e9 / hbm_peak, 4)},
+        "gpu_launches": per_step_launches * args.steps if per_step_launches > 0 else None,
+        "launches_per_step": per_step_launches,
+        "e2e": e2e,
+        "clocks": clk,
+        "batch32": batch,
+    }
+    return line
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_step(wl):
+    import oracle
+    return oracle.decode(W.bits(wl.q_idx), wl.w_idx.numpy(), W.bits(wl.k_idx), W.bits(wl.comp_kv),
+                         W.bits(wl.swa_kv), W.bits(wl.q), wl.tok_seq.numpy(), wl.tok_pos.numpy(),
+                         wl.comp_off.numpy(), wl.swa_first_pos.numpy(), top_k=wl.top_k,
+                         window=wl.window, ratio=wl.ratio, scale=wl.scale)
+
+
+def cpu_baseline(steps: int):
+    """The oracle as it stands, on full 1M decode steps (one token, one layer each)."""
+    import oracle
+    oracle.build()
+    wl = W.ctx1m(seed=0)
+    oracle_step(wl)   # warm (page in)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(wl)
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(1.0 / dt, 4), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{steps} full 1m decode steps (262144 blocks, top_k 1024, 64 heads), f64"}
+
+
+class OracleSlices:
+    """The oracle's decode of one 1m token, cut into `m` steps: steps 0..m-1
+    each score a contiguous slice of the blocks (the oracle's indexer on a
+    sub-range of the cache); the last one also runs the oracle's top-k, mixed
+    gather and attention on the whole score row.  m steps = one token."""
+
+    def __init__(self, wl, m: int):
+        import oracle
+        self.o = oracle
+        self.wl = wl
+        self.m = m
+        n = int(wl.comp_off[1])
+        self.n = n
+        self.cuts = [n * i // m for i in range(m + 1)]
+        self.scores = np.zeros(n)
+        self.qb, self.kb = W.bits(wl.q_idx), W.bits(wl.k_idx)
+        self.w = wl.w_idx.numpy()
+        self.i = 0
+
+    def step(self):
+        o, wl = self.o, self.wl
+        j = self.i % self.m
+        a, b = self.cuts[j], self.cuts[j + 1]
+        if b > a:
+            sc, _ = o.indexer_scores(self.qb, self.w, self.kb, [0], [4 * (b - a)], [a, b])
+            self.scores[a:b] = sc[0, : b - a]
+        if j == self.m - 1:
+            idx, ns = o.topk(self.scores, wl.top_k)
+            kv, kl = o.gather(idx[None], np.array([ns], np.int32), W.bits(wl.comp_kv),
+                              W.bits(wl.swa_kv), wl.tok_seq.numpy(), wl.tok_pos.numpy(),
+                              wl.comp_off.numpy(), wl.swa_first_pos.numpy(), top_k=wl.top_k,
+                              window=wl.window, ratio=wl.ratio)
+            o.attention(W.bits(wl.q), kv, kl, wl.scale)
+        self.i += 1
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed on this workload, K steps after W.
+    A step is 1/m of one token's decode, m sized so the run takes ~2-3 minutes."""
+    import oracle
+    oracle.build()
+    wl = W.ctx1m(seed=0)
+    per_token_s = 2.0                      # ~1.6 s measured on 8 cores; a generous bound
+    m = max(1, int(np.ceil((args.steps + args.warmup) * per_token_s / 150.0)))
+    sl = OracleSlices(wl, m)
+    for _ in range(args.warmup):
+        sl.step()
+    sl.i = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sl.step()
+    dt = time.perf_counter() - t0
+    v = round((args.steps / m) / dt, 4)
+    sample = (f"each step = 1/{m} of one full 1m decode token (indexer over a contiguous "
+              f"1/{m} of the 262144 blocks; every {m}th step also top-k, gather, attention); "
+              f"value = (steps/{m}) tokens / time")
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "1m: CSA decode, 1 token, 262144 blocks (64 MiB keys, 256 MiB "
+                               "rows), top_k 1024, window 128, 64 heads, hd 512, 32 planted",
+                   "slices_per_token": m},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--cpu-steps", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-batch32", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        # the oracle arm runs on rank 0 only; the other ranks exit without work
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    line = run_ours(args, rank, world, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_steps)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

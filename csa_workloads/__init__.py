@@ -89,7 +89,8 @@ class Workload:
 
 
 def bf16_normal(gen: torch.Generator, *shape) -> torch.Tensor:
-    return torch.randn(*shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    return torch.randn(*shape, generator=gen, dtype=torch.float32,
+                       device=gen.device).to(torch.bfloat16)
 
 
 def bits(t: torch.Tensor):
@@ -100,8 +101,8 @@ def bits(t: torch.Tensor):
 def make(name: str = "custom", *, seed: int = 0, seq_lens=None, tokens=None,
          n_comp=None, top_k: int = 64, n_heads: int = 16, n_ih: int = N_IH, ihd: int = IHD,
          hd: int = HD, window: int = WINDOW, ratio: int = RATIO, swa_cap: Optional[int] = None,
-         comp_capacity=None, scale: Optional[float] = None, w_scale: float = 1.0 / 8.0
-         ) -> Workload:
+         comp_capacity=None, scale: Optional[float] = None, w_scale: float = 1.0 / 8.0,
+         device=None) -> Workload:
     """A general seeded workload.
 
     seq_lens[b]   absolute position of the first query token of sequence b
@@ -110,8 +111,9 @@ def make(name: str = "custom", *, seed: int = 0, seq_lens=None, tokens=None,
     n_comp[b]     compressed blocks in the cache (default: every complete block
                   before the last query token, i.e. floor(last_pos / ratio));
     comp_capacity rows reserved per sequence (>= n_comp; extra rows are drawn too).
+    device        draw the data tensors there (default: the CPU generator).
     """
-    gen = torch.Generator().manual_seed(seed)
+    gen = torch.Generator(device=device or "cpu").manual_seed(seed)
     if seq_lens is None:
         seq_lens = [1024]
     B = len(seq_lens)
@@ -147,7 +149,7 @@ def make(name: str = "custom", *, seed: int = 0, seq_lens=None, tokens=None,
     comp_kv = bf16_normal(gen, R, hd)
     swa_kv = bf16_normal(gen, B, swa_cap, hd)
     q_idx = bf16_normal(gen, T, n_ih, ihd)
-    w_idx = torch.randn(T, n_ih, generator=gen, dtype=torch.float32) * w_scale
+    w_idx = torch.randn(T, n_ih, generator=gen, dtype=torch.float32, device=gen.device) * w_scale
     q = bf16_normal(gen, T, n_heads, hd)
     # oldest position still resident in each ring: the ring holds the last
     # swa_cap positions up to the last query token of the sequence.
@@ -178,6 +180,7 @@ def plant_blocks(wl: Workload, count: int = 32, factor: float = 4.0, seed: int =
     n0 = int(wl.comp_off[1] - wl.comp_off[0])
     base = int(wl.comp_off[0])
     picks = torch.randperm(n0, generator=gen)[:count].sort().values.to(torch.int64)
+    picks = picks.to(wl.k_idx.device)
     qf = wl.q_idx[0].float()                      # [n_ih, ihd]
     wpos = wl.w_idx[0].clamp_min(0.0)             # [n_ih]
     mu = (wpos[:, None] * qf).sum(0)
@@ -185,7 +188,7 @@ def plant_blocks(wl: Workload, count: int = 32, factor: float = 4.0, seed: int =
     for s in picks.tolist():
         k = wl.k_idx[base + s].float()
         wl.k_idx[base + s] = (factor * k.norm() * mu).to(torch.bfloat16)
-    wl.planted = picks
+    wl.planted = picks.cpu()
     return wl
 
 
@@ -223,12 +226,12 @@ def ctx64k_step(wl: Workload, i: int, gen: torch.Generator) -> None:
     wl.q.copy_(bf16_normal(gen, *wl.q.shape))
 
 
-def ctx1m(seed: int = 0, planted: int = 32) -> Workload:
+def ctx1m(seed: int = 0, planted: int = 32, device=None) -> Workload:
     """1M-context single-sequence decode on one CSA layer: 262,144 blocks
     (64 MiB of indexer keys, 256 MiB of rows), top_k 1024, 64 heads, 32
     planted blocks."""
     wl = make("1m", seed=seed, seq_lens=[1 << 20], tokens=[1], n_comp=[262144], top_k=1024,
-              n_heads=64, swa_cap=128)
+              n_heads=64, swa_cap=128, device=device)
     if planted:
         plant_blocks(wl, planted, 4.0, seed + 1)
     return wl
@@ -239,21 +242,22 @@ def batch32_lens(seed: int = 0, n: int = 32):
     return torch.randint(32768, 131072 + 1, (n,), generator=gen).tolist()
 
 
-def batch32(seed: int = 0) -> Workload:
+def batch32(seed: int = 0, device=None) -> Workload:
     """32 sequences with context lengths uniform in 32K..128K; one query token
     per sequence at position len; n_comp = len // 4, packed with offsets."""
     lens = batch32_lens(seed)
     return make("batch32", seed=seed, seq_lens=lens, tokens=[1] * len(lens),
-                n_comp=[l // 4 for l in lens], top_k=1024, n_heads=64, swa_cap=128)
+                n_comp=[l // 4 for l in lens], top_k=1024, n_heads=64, swa_cap=128,
+                device=device)
 
 
-def prefill(seed: int = 0, tokens: int = 4096) -> Workload:
+def prefill(seed: int = 0, tokens: int = 4096, device=None) -> Workload:
     """Chunked prefill: `tokens` query tokens at positions 262144 .. of one
     sequence, 66,559 cached blocks (every block any token of the 4096 chunk
     can see), a ring of 8192 window rows covering positions 262017 onwards."""
     last = 262144 + tokens - 1
     return make("prefill", seed=seed, seq_lens=[262144], tokens=[tokens],
-                n_comp=[last // 4], top_k=1024, n_heads=64, swa_cap=8192)
+                n_comp=[last // 4], top_k=1024, n_heads=64, swa_cap=8192, device=device)
 
 
 NAMED = {"tiny": tiny, "64k": ctx64k, "1m": ctx1m, "batch32": batch32, "prefill": prefill}

@@ -1,0 +1,330 @@
+// csa_api.cu -- the C ABI of libcsa.so (declared in include/csa.h).
+//
+// Host side only: argument validation, the workspace plan, tensor-map
+// encoding and kernel launches.  Nothing here allocates, frees or
+// synchronises; every device buffer belongs to the caller.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <mutex>
+
+#include "csa_device.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p) {
+    WsPlan w;
+    w.T = T;
+    w.top_k = p.top_k;
+    w.H = p.n_heads;
+    w.ld = ((max_comp_rows > 0 ? max_comp_rows : 1) + 3) / 4 * 4;
+    w.cap = T <= 64 ? 8192 : 1024;
+    // Attention split: enough CTAs for ~2 waves, at most 64 splits per token.
+    const int64_t rows_max = static_cast<int64_t>(p.top_k) + p.window;
+    const int64_t chunks = (rows_max + kAttnChunk - 1) / kAttnChunk;
+    const int64_t ctas = (T > 0 ? T : 1) * (p.n_heads / kHeadGroup);
+    int64_t splits = (kTargetCtas + ctas - 1) / ctas;
+    if (splits > chunks) splits = chunks;
+    if (splits > 64) splits = 64;
+    if (splits < (chunks + 63) / 64) splits = (chunks + 63) / 64;
+    if (splits < 1) splits = 1;
+    const int64_t per = (chunks + splits - 1) / splits;
+    w.rows_split = static_cast<int32_t>(per * kAttnChunk);
+    w.splits = static_cast<int32_t>((rows_max + w.rows_split - 1) / w.rows_split);
+    const size_t A = 256;
+    const size_t Tz = static_cast<size_t>(T > 0 ? T : 0);
+    w.state_bytes = Tz * kStateWords * 4;
+    size_t off = 0;
+    w.off_scores = off;  off = align_up(off + Tz * w.ld * 4, A);
+    w.off_sel = off;     off = align_up(off + Tz * p.top_k * 4, A);
+    w.off_cand = off;    off = align_up(off + Tz * w.cap * 8, A);
+    w.off_idx = off;     off = align_up(off + Tz * p.top_k * 4, A);
+    w.off_nsel = off;    off = align_up(off + Tz * 4, A);
+    w.off_part_o = off;
+    if (w.splits > 1) off = align_up(off + Tz * w.splits * w.H * kHD * 4, A);
+    w.off_part_ml = off;
+    if (w.splits > 1) off = align_up(off + Tz * w.splits * w.H * 2 * 4, A);
+    w.data_bytes = off;
+    w.total = w.state_bytes + w.data_bytes + A;
+    return w;
+}
+
+// Start of the data area: packed against the end of the caller's workspace.
+static uint8_t *data_base(void *ws, size_t ws_bytes, const WsPlan &plan) {
+    const size_t off = (ws_bytes - plan.data_bytes) & ~static_cast<size_t>(255);
+    return static_cast<uint8_t *>(ws) + off;
+}
+
+// ---------------------------------------------------------------- driver entry point
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+CUresult encode_tensor_map_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
+                                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                                   uint32_t box_outer) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return CUDA_ERROR_NOT_SUPPORTED;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// ---------------------------------------------------------------- device check
+
+static int g_dev_ok[64];          // 0 unknown, 1 ok, -1 unsupported
+static int g_dev_sms[64];
+static std::mutex g_dev_mu;
+
+static csa_status_t current_device(int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return CSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev_ok[dev] == 0) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return CSA_ERR_CUDA;
+        // Kernels are built for sm_103a only.
+        g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        g_dev_sms[dev] = n;
+    }
+    if (g_dev_ok[dev] < 0) return CSA_ERR_UNSUPPORTED;
+    *sms = g_dev_sms[dev];
+    return CSA_OK;
+}
+
+}  // namespace csa
+
+using namespace csa;
+
+// ---------------------------------------------------------------- validation
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static csa_status_t check_params(const csa_params_t *p) {
+    if (!p) return CSA_ERR_INVALID_ARGUMENT;
+    if (p->n_ih != kNIH || p->ihd != kIHD || p->hd != kHD) return CSA_ERR_UNSUPPORTED;
+    if (p->n_heads < kHeadGroup || p->n_heads > 128 || p->n_heads % kHeadGroup) return CSA_ERR_UNSUPPORTED;
+    if (p->top_k < 1) return CSA_ERR_INVALID_ARGUMENT;
+    if (p->top_k > kMaxTopK) return CSA_ERR_UNSUPPORTED;
+    if (p->window < 1 || p->ratio < 1) return CSA_ERR_INVALID_ARGUMENT;
+    if (!isfinite(p->scale)) return CSA_ERR_INVALID_ARGUMENT;
+    return CSA_OK;
+}
+
+static csa_status_t check_layout(const csa_layout_t *L, const csa_params_t *p, bool need_swa) {
+    if (!L) return CSA_ERR_INVALID_ARGUMENT;
+    if (L->num_seqs < 1 || L->num_tokens < 0) return CSA_ERR_INVALID_ARGUMENT;
+    if (L->total_comp_rows < 0 || L->max_comp_rows < 0) return CSA_ERR_INVALID_ARGUMENT;
+    if (L->max_comp_rows > L->total_comp_rows) return CSA_ERR_INVALID_ARGUMENT;
+    if (L->total_comp_rows >= (int64_t(1) << 31)) return CSA_ERR_UNSUPPORTED;
+    if (L->num_tokens > 0 && (!L->tok_seq || !L->tok_pos || !L->comp_off))
+        return CSA_ERR_INVALID_ARGUMENT;
+    // indexer work units: one token, or 4 tokens of a single sequence
+    const int64_t units = (L->num_seqs == 1 && L->num_tokens >= 4) ? (L->num_tokens + 3) / 4
+                                                                   : L->num_tokens;
+    if (units > 4096) return CSA_ERR_UNSUPPORTED;
+    if (need_swa && L->num_tokens > 0) {
+        if (!L->swa_kv || !L->swa_first_pos) return CSA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(L->swa_kv)) return CSA_ERR_INVALID_ARGUMENT;
+        if (L->swa_cap < p->window) return CSA_ERR_CAPACITY;
+    }
+    return CSA_OK;
+}
+
+static csa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+static csa_status_t check_ws(const WsPlan &plan, void *ws, size_t ws_bytes) {
+    if (plan.total > 0 && !ws) return CSA_ERR_WORKSPACE;
+    if (ws_bytes < plan.total) return CSA_ERR_WORKSPACE;
+    if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return CSA_ERR_INVALID_ARGUMENT;
+    return CSA_OK;
+}
+
+#define CSA_TRY(x)                          \
+    do {                                    \
+        csa_status_t _s = (x);              \
+        if (_s != CSA_OK) return _s;        \
+    } while (0)
+
+extern "C" {
+
+const char *csa_status_string(csa_status_t s) {
+    switch (s) {
+        case CSA_OK: return "CSA_OK";
+        case CSA_ERR_INVALID_ARGUMENT: return "CSA_ERR_INVALID_ARGUMENT";
+        case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED";
+        case CSA_ERR_CAPACITY: return "CSA_ERR_CAPACITY";
+        case CSA_ERR_CUDA: return "CSA_ERR_CUDA";
+        case CSA_ERR_DEVICE_FAULT: return "CSA_ERR_DEVICE_FAULT";
+        case CSA_ERR_TIMEOUT: return "CSA_ERR_TIMEOUT";
+        case CSA_ERR_WORKSPACE: return "CSA_ERR_WORKSPACE";
+    }
+    return "CSA_ERR_UNKNOWN";
+}
+
+int32_t csa_abi_version(void) { return CSA_ABI_VERSION; }
+
+csa_status_t csa_workspace_size(const csa_layout_t *layout, const csa_params_t *params,
+                                size_t *bytes) {
+    if (!bytes) return CSA_ERR_INVALID_ARGUMENT;
+    CSA_TRY(check_params(params));
+    if (!layout) return CSA_ERR_INVALID_ARGUMENT;
+    if (layout->num_tokens < 0 || layout->max_comp_rows < 0) return CSA_ERR_INVALID_ARGUMENT;
+    *bytes = make_plan(layout->num_tokens, layout->max_comp_rows, *params).total;
+    return CSA_OK;
+}
+
+csa_status_t csa_indexer_scores(const csa_layout_t *layout, const csa_params_t *params,
+                                const void *q_idx, const float *w_idx, const void *k_idx,
+                                float *scores, int64_t ld_scores, int32_t *dev_status,
+                                void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, false));
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!q_idx || !w_idx || !scores || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (layout->total_comp_rows > 0 && !k_idx) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q_idx) || (k_idx && !aligned16(k_idx))) return CSA_ERR_INVALID_ARGUMENT;
+    if (ld_scores < layout->max_comp_rows || ld_scores < 1) return CSA_ERR_CAPACITY;
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    return cuda_status(launch_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores,
+                                      ld_scores, nullptr, dev_status));
+}
+
+csa_status_t csa_topk(const csa_layout_t *layout, const csa_params_t *params, const float *scores,
+                      int64_t ld_scores, int32_t *idx, int32_t *n_sel, int32_t *dev_status,
+                      void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, false));
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!scores || !idx || !n_sel || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (ld_scores < layout->max_comp_rows || ld_scores < 1) return CSA_ERR_CAPACITY;
+    const WsPlan plan = make_plan(layout->num_tokens, layout->max_comp_rows, *params);
+    CSA_TRY(check_ws(plan, ws, ws_bytes));
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    uint8_t *w = data_base(ws, ws_bytes, plan);
+    TopkWs tw{static_cast<uint32_t *>(ws), reinterpret_cast<int32_t *>(w + plan.off_sel),
+              reinterpret_cast<uint64_t *>(w + plan.off_cand), plan.cap};
+    return cuda_status(launch_topk(lc, *layout, *params, scores, ld_scores, tw, false, idx, n_sel,
+                                   dev_status));
+}
+
+csa_status_t csa_gather_mixed(const csa_layout_t *layout, const csa_params_t *params,
+                              const int32_t *idx, const int32_t *n_sel, const void *comp_kv,
+                              void *kv_buf, int32_t *kv_len, int32_t *dev_status, void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, true));
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!idx || !n_sel || !kv_buf || !kv_len || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (layout->total_comp_rows > 0 && !comp_kv) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(kv_buf) || (comp_kv && !aligned16(comp_kv))) return CSA_ERR_INVALID_ARGUMENT;
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    RowSource R{};
+    R.fused = 1;
+    R.rows_per_token = params->top_k + params->window;
+    R.L = *layout;
+    R.ratio = params->ratio;
+    R.window = params->window;
+    R.top_k = params->top_k;
+    R.idx = idx;
+    R.n_sel = n_sel;
+    R.comp_kv = comp_kv;
+    return cuda_status(launch_gather(lc, R, layout->num_tokens, kv_buf, kv_len, dev_status));
+}
+
+csa_status_t csa_sparse_mqa_decode(int32_t num_tokens, const csa_params_t *params, const void *q,
+                                   const void *kv_buf, const int32_t *kv_len, const float *sinks,
+                                   float *out, int32_t *dev_status, void *ws, size_t ws_bytes,
+                                   void *stream) {
+    CSA_TRY(check_params(params));
+    if (num_tokens < 0) return CSA_ERR_INVALID_ARGUMENT;
+    if (num_tokens == 0) return CSA_OK;
+    if (!q || !kv_buf || !kv_len || !out || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(kv_buf) || !aligned16(out)) return CSA_ERR_INVALID_ARGUMENT;
+    const WsPlan plan = make_plan(num_tokens, 0, *params);
+    CSA_TRY(check_ws(plan, ws, ws_bytes));
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    RowSource R{};
+    R.fused = 0;
+    R.kv_buf = kv_buf;
+    R.kv_len = kv_len;
+    R.rows_per_token = params->top_k + params->window;
+    uint8_t *w = data_base(ws, ws_bytes, plan);
+    return cuda_status(launch_attention(lc, R, num_tokens, *params, plan, q, sinks, out,
+                                        reinterpret_cast<float *>(w + plan.off_part_o),
+                                        reinterpret_cast<float *>(w + plan.off_part_ml),
+                                        dev_status));
+}
+
+csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, const void *q_idx,
+                        const float *w_idx, const void *k_idx, const void *comp_kv, const void *q,
+                        const float *sinks, float *out, int32_t *idx_out, int32_t *dev_status,
+                        void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, true));
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!q_idx || !w_idx || !q || !out || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (layout->total_comp_rows > 0 && (!k_idx || !comp_kv)) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q_idx) || !aligned16(q) || !aligned16(out) ||
+        (k_idx && !aligned16(k_idx)) || (comp_kv && !aligned16(comp_kv)))
+        return CSA_ERR_INVALID_ARGUMENT;
+    const WsPlan plan = make_plan(layout->num_tokens, layout->max_comp_rows, *params);
+    CSA_TRY(check_ws(plan, ws, ws_bytes));
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    uint8_t *w = data_base(ws, ws_bytes, plan);
+    float *scores = reinterpret_cast<float *>(w + plan.off_scores);
+    uint32_t *state = static_cast<uint32_t *>(ws);
+    int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(w + plan.off_idx);
+    int32_t *nsel = reinterpret_cast<int32_t *>(w + plan.off_nsel);
+    const bool fuse = indexer_fuses_hist(*layout);
+    cudaError_t e = launch_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores, plan.ld,
+                                   fuse ? state : nullptr, dev_status);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+    TopkWs tw{state, reinterpret_cast<int32_t *>(w + plan.off_sel),
+              reinterpret_cast<uint64_t *>(w + plan.off_cand), plan.cap};
+    e = launch_topk(lc, *layout, *params, scores, plan.ld, tw, fuse, idx, nsel, dev_status);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+    RowSource R{};
+    R.fused = 1;
+    R.rows_per_token = params->top_k + params->window;
+    R.L = *layout;
+    R.ratio = params->ratio;
+    R.window = params->window;
+    R.top_k = params->top_k;
+    R.idx = idx;
+    R.n_sel = nsel;
+    R.comp_kv = comp_kv;
+    return cuda_status(launch_attention(lc, R, layout->num_tokens, *params, plan, q, sinks, out,
+                                        reinterpret_cast<float *>(w + plan.off_part_o),
+                                        reinterpret_cast<float *>(w + plan.off_part_ml),
+                                        dev_status));
+}
+
+}  // extern "C"

@@ -1,0 +1,450 @@
+// csa_attention.cu -- mixed gather and shared-KV multi-query attention.
+//
+// Rows attended by token t ("ARCHITECTURE & MEMORY AUDIT -- 1M-context
+// viability", D3 and D5; "PART A -- Next Session Clues", section 3): the
+// selected compressed rows in index order, then the sliding-window rows
+// oldest first, both kept where they overlap.  Each 512-wide row is the key
+// and the value of every query head (shared-KV MQA).
+//
+// Attention is a split-KV flash decode.  A CTA owns one token, 16 query heads
+// and a contiguous range of rows, which it walks in chunks of 32 rows: the
+// rows are fetched with 16-byte cp.async (straight from the compressed cache
+// by index and from the window ring in fused mode, "1M-context viability",
+// M5), QK^T and PV run on mma.sync bf16 tensor-core tiles with f32
+// accumulation, and the softmax is online across chunks with warp-shuffle
+// reductions.  Each row is read once for all 16 heads of the CTA.  With more
+// than one split per token, a combine kernel merges the partial (m, l, O)
+// with log-sum-exp weights.
+#include <math.h>
+
+#include "csa_device.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+
+constexpr int kAttnThreads = 128;
+constexpr int kRowBytes = kHD * 2;  // 1 KiB
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Row count of token t and the address of its row j (nullptr: skipped row).
+struct TokRows {
+    int32_t len;
+    int32_t n_sel;
+    int64_t first;  // first window position (fused)
+    int64_t n_vis;
+    int64_t off;
+    int b;
+    int bad;
+};
+
+__device__ __forceinline__ TokRows token_rows(const RowSource &R, int t) {
+    TokRows r;
+    r.n_sel = 0;
+    r.first = 0;
+    r.n_vis = 0;
+    r.off = 0;
+    r.b = 0;
+    r.bad = 0;
+    if (!R.fused) {
+        int32_t len = R.kv_len[t];
+        if (len < 0 || len > R.rows_per_token) {
+            r.bad = CSA_DEV_BAD_LENGTH;
+            len = len < 0 ? 0 : R.rows_per_token;
+        }
+        r.len = len;
+        return r;
+    }
+    TokenView v = token_view(R.L, R.ratio, t);
+    r.bad = v.bad;
+    if (v.bad & CSA_DEV_BAD_LAYOUT) {
+        r.len = 0;
+        return r;
+    }
+    int32_t ns = R.n_sel[t];
+    if (ns < 0 || ns > R.top_k) {
+        r.bad |= CSA_DEV_BAD_LENGTH;
+        ns = ns < 0 ? 0 : R.top_k;
+    }
+    r.n_sel = ns;
+    r.first = window_first(v.pos, R.window);
+    r.n_vis = v.n_vis;
+    r.off = v.off;
+    r.b = v.b;
+    r.len = ns + static_cast<int32_t>(v.pos - r.first + 1);
+    return r;
+}
+
+__device__ __forceinline__ const __nv_bfloat16 *row_ptr(const RowSource &R, const TokRows &tr,
+                                                         int t, int j, int *bad) {
+    if (!R.fused)
+        return static_cast<const __nv_bfloat16 *>(R.kv_buf) +
+               (static_cast<int64_t>(t) * R.rows_per_token + j) * kHD;
+    if (j < tr.n_sel) {
+        const int32_t s = R.idx[static_cast<int64_t>(t) * R.top_k + j];
+        if (s < 0 || s >= tr.n_vis) {
+            *bad |= CSA_DEV_BAD_INDEX;
+            return nullptr;
+        }
+        return static_cast<const __nv_bfloat16 *>(R.comp_kv) + (tr.off + s) * kHD;
+    }
+    const int64_t x = tr.first + (j - tr.n_sel);
+    if (x < R.L.swa_first_pos[tr.b]) {
+        *bad |= CSA_DEV_MISSING_SWA;
+        return nullptr;
+    }
+    const int64_t slot = x % R.L.swa_cap;
+    return static_cast<const __nv_bfloat16 *>(R.L.swa_kv) +
+           (static_cast<int64_t>(tr.b) * R.L.swa_cap + slot) * kHD;
+}
+
+// ---------------------------------------------------------------- gather
+
+__global__ void __launch_bounds__(256) gather_kernel(const RowSource R, __nv_bfloat16 *kv_buf,
+                                                     int32_t *kv_len, int32_t *status) {
+    pdl_wait();
+    const int t = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = blockIdx.x * 8 + warp;
+    const TokRows tr = token_rows(R, t);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        kv_len[t] = tr.len;
+        raise_status(status, tr.bad);
+    }
+    if (j < tr.len) {
+        int bad = 0;
+        const __nv_bfloat16 *src = row_ptr(R, tr, t, j, &bad);
+        uint4 *dst = reinterpret_cast<uint4 *>(kv_buf + (static_cast<int64_t>(t) * R.rows_per_token + j) * kHD);
+        if (src) {
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+            const uint4 a = __ldg(s4 + lane), b = __ldg(s4 + lane + 32);
+            dst[lane] = a;
+            dst[lane + 32] = b;
+        } else {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            dst[lane] = z;
+            dst[lane + 32] = z;
+            if (lane == 0) raise_status(status, bad);
+        }
+    }
+    pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------- attention
+
+struct AttnParams {
+    RowSource R;
+    int32_t H;
+    int32_t splits;
+    int32_t rows_split;
+    float scale_log2;        // scale * log2(e)
+    const __nv_bfloat16 *q;  // [T][H][512]
+    const float *sinks;      // [H] or null
+    float *out;              // [T][H][512]
+    float *part_o;           // [T][splits][H][512]
+    float *part_ml;          // [T][splits][H][2]  (m in log2 units, l)
+    int32_t *status;
+};
+
+struct AttnSmem {
+    __nv_bfloat16 q[kHeadGroup * kHD];              // 16 KiB, 16-byte chunks xor-swizzled by row
+    __nv_bfloat16 rows[2][kAttnChunk * kHD];        // 2 x 32 KiB, same swizzle
+    const __nv_bfloat16 *ptr[2][kAttnChunk];
+    float s[kHeadGroup][kAttnChunk];                // logits of the chunk (log2 units)
+    __nv_bfloat16 p[kHeadGroup][kAttnChunk + 8];    // probabilities, padded rows
+    float m[kHeadGroup], l[kHeadGroup], alpha[kHeadGroup];
+    TokRows tr;
+};
+
+// 16-byte chunk c of row r lives at chunk (c ^ (r & 7)): ldmatrix of 8 rows at
+// one column then touches 8 distinct bank groups.
+__device__ __forceinline__ uint32_t swz(int r, int chunk) {
+    return static_cast<uint32_t>(r * kRowBytes + ((chunk ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void issue_chunk(AttnSmem &S, const RowSource &R, int t, int buf,
+                                            int r0, int r_end, int *bad) {
+    // pointers of the 32 rows (warp 0), then 32 x 64 16-byte copies (all threads)
+    if (threadIdx.x < kAttnChunk) {
+        const int j = r0 + threadIdx.x;
+        S.ptr[buf][threadIdx.x] = j < r_end ? row_ptr(R, S.tr, t, j, bad) : nullptr;
+    }
+    __syncthreads();
+    uint8_t *base = reinterpret_cast<uint8_t *>(S.rows[buf]);
+    for (int i = threadIdx.x; i < kAttnChunk * 64; i += kAttnThreads) {
+        const int r = i >> 6, c = i & 63;
+        const __nv_bfloat16 *src = S.ptr[buf][r];
+        cp_async16(base + swz(r, c), src ? static_cast<const void *>(src + c * 8) : R.comp_kv ? R.comp_kv : R.kv_buf,
+                   src != nullptr);
+    }
+    cp_async_commit();
+}
+
+__global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParams A) {
+    extern __shared__ uint8_t smem_raw[];
+    AttnSmem &S = *reinterpret_cast<AttnSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int split = blockIdx.x, hg = blockIdx.y, t = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+
+    pdl_wait();
+    if (threadIdx.x == 0) S.tr = token_rows(A.R, t);
+    __syncthreads();
+    const int len = S.tr.len;
+    const int r_begin = split * A.rows_split;
+    const int r_end = min(len, r_begin + A.rows_split);
+    int bad = (threadIdx.x == 0 && split == 0 && hg == 0) ? S.tr.bad : 0;
+
+    if (r_begin >= r_end) {
+        // nothing here; with one split this CTA still owns the output (zeros)
+        if (A.splits == 1) {
+            float *o = A.out + (static_cast<int64_t>(t) * A.H + hg * kHeadGroup) * kHD;
+            for (int i = threadIdx.x; i < kHeadGroup * kHD; i += kAttnThreads) o[i] = 0.f;
+        }
+        raise_status(A.status, bad);
+        pdl_launch_dependents();
+        return;
+    }
+
+    // q of this head group
+    {
+        const __nv_bfloat16 *qg = A.q + (static_cast<int64_t>(t) * A.H + hg * kHeadGroup) * kHD;
+        uint8_t *qs = reinterpret_cast<uint8_t *>(S.q);
+        for (int i = threadIdx.x; i < kHeadGroup * 64; i += kAttnThreads) {
+            const int r = i >> 6, ch = i & 63;
+            cp_async16(qs + swz(r, ch), qg + r * kHD + ch * 8, true);
+        }
+        cp_async_commit();
+    }
+    if (threadIdx.x < kHeadGroup) {
+        S.m[threadIdx.x] = -INFINITY;
+        S.l[threadIdx.x] = 0.f;
+    }
+    const int nchunks = (r_end - r_begin + kAttnChunk - 1) / kAttnChunk;
+    issue_chunk(S, A.R, t, 0, r_begin, r_end, &bad);
+
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    const uint32_t q_base = smem_addr(S.q);
+    const uint32_t p_base = smem_addr(&S.p[0][0]);
+
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int buf = ci & 1;
+        const int r0 = r_begin + ci * kAttnChunk;
+        if (ci + 1 < nchunks) {
+            issue_chunk(S, A.R, t, buf ^ 1, r0 + kAttnChunk, r_end, &bad);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const uint32_t rows_base = smem_addr(S.rows[buf]);
+
+        // ---- logits: warp w owns rows 8w..8w+7 of the chunk, all 16 heads
+        {
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int rr = warp * 8 + (lane & 7);
+#pragma unroll 4
+            for (int kk = 0; kk < kHD / 16; kk += 2) {
+                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                ldsm_x4(q_base + swz(qr, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+                ldsm_x4(rows_base + swz(rr, kk * 2 + (lane >> 3)), b0, b1, b2, b3);
+                mma_bf16_16816(sacc, a0, a1, a2, a3, b0, b1);
+                ldsm_x4(q_base + swz(qr, (kk + 1) * 2 + (lane >> 4)), a0, a1, a2, a3);
+                mma_bf16_16816(sacc, a0, a1, a2, a3, b2, b3);
+            }
+            // c-fragment: heads g, g+8; rows 2c, 2c+1 of this warp's 8
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int head = g + (e >> 1) * 8;
+                const int col = warp * 8 + 2 * c + (e & 1);
+                const bool valid = r0 + col < r_end && S.ptr[buf][col] != nullptr;
+                S.s[head][col] = valid ? sacc[e] * A.scale_log2 : -INFINITY;
+            }
+        }
+        __syncthreads();
+
+        // ---- online softmax: warp w owns heads 4w..4w+3, lane = row
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+            const int h = warp * 4 + hh;
+            const float x = S.s[h][lane];
+            float mx = x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_old = S.m[h];
+            const float m_new = fmaxf(m_old, mx);
+            const float p = (x == -INFINITY) ? 0.f : exp2f(x - m_new);
+            float sum = p;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+            S.p[h][lane] = __float2bfloat16_rn(p);
+            __syncwarp();
+            if (lane == 0) {
+                S.l[h] = S.l[h] * alpha + sum;
+                S.m[h] = m_new;
+                S.alpha[h] = alpha;
+            }
+        }
+        __syncthreads();
+
+        // ---- O = alpha O + P V: warp w owns columns 128w .. 128w+127
+        {
+            const float al0 = S.alpha[g], al1 = S.alpha[g + 8];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] *= al0;
+                o[i][1] *= al0;
+                o[i][2] *= al1;
+                o[i][3] *= al1;
+            }
+#pragma unroll
+            for (int ks = 0; ks < kAttnChunk / 16; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                const int pr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int pc = ks * 16 + (lane >> 4) * 8;
+                ldsm_x4(p_base + static_cast<uint32_t>((pr * (kAttnChunk + 8) + pc) * 2), a0, a1, a2, a3);
+                const int vr = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    const int chunk = (warp * 128 + np * 16) / 8 + (lane >> 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(rows_base + swz(vr, chunk), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- write
+    const int h0 = hg * kHeadGroup;
+    if (A.splits == 1) {
+        float z0 = S.l[g], z1 = S.l[g + 8];
+        if (A.sinks) {
+            z0 += exp2f(A.sinks[h0 + g] * kLog2e - S.m[g]);
+            z1 += exp2f(A.sinks[h0 + g + 8] * kLog2e - S.m[g + 8]);
+        }
+        const float inv0 = z0 > 0.f ? 1.f / z0 : 0.f, inv1 = z1 > 0.f ? 1.f / z1 : 0.f;
+        float *o0 = A.out + (static_cast<int64_t>(t) * A.H + h0 + g) * kHD + warp * 128 + 2 * c;
+        float *o1 = o0 + 8 * kHD;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            *reinterpret_cast<float2 *>(o0 + i * 8) = make_float2(o[i][0] * inv0, o[i][1] * inv0);
+            *reinterpret_cast<float2 *>(o1 + i * 8) = make_float2(o[i][2] * inv1, o[i][3] * inv1);
+        }
+    } else {
+        const int64_t pbase = (static_cast<int64_t>(t) * A.splits + split) * A.H + h0;
+        float *o0 = A.part_o + (pbase + g) * kHD + warp * 128 + 2 * c;
+        float *o1 = o0 + 8 * kHD;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            *reinterpret_cast<float2 *>(o0 + i * 8) = make_float2(o[i][0], o[i][1]);
+            *reinterpret_cast<float2 *>(o1 + i * 8) = make_float2(o[i][2], o[i][3]);
+        }
+        if (threadIdx.x < kHeadGroup) {
+            A.part_ml[(pbase + threadIdx.x) * 2 + 0] = S.m[threadIdx.x];
+            A.part_ml[(pbase + threadIdx.x) * 2 + 1] = S.l[threadIdx.x];
+        }
+    }
+    raise_status(A.status, bad);
+    pdl_launch_dependents();
+}
+
+// out[t,h,:] = sum_s 2^(m_s - M) O_s / (sum_s 2^(m_s - M) l_s [+ 2^(sink*log2e - M)])
+__global__ void __launch_bounds__(128) combine_kernel(const AttnParams A) {
+    pdl_wait();
+    const int h = blockIdx.x, t = blockIdx.y;
+    __shared__ float wgt[64];
+    __shared__ float inv_z;
+    const TokRows tr = token_rows(A.R, t);
+    const int nsp = min(A.splits, (tr.len + A.rows_split - 1) / A.rows_split);
+    float *o = A.out + (static_cast<int64_t>(t) * A.H + h) * kHD;
+    if (nsp <= 0) {
+        for (int i = threadIdx.x; i < kHD; i += blockDim.x) o[i] = 0.f;
+        pdl_launch_dependents();
+        return;
+    }
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        float M = -INFINITY;
+        for (int s = lane; s < nsp; s += 32)
+            M = fmaxf(M, A.part_ml[((static_cast<int64_t>(t) * A.splits + s) * A.H + h) * 2]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float sink = A.sinks ? A.sinks[h] * kLog2e : -INFINITY;
+        const float Mall = fmaxf(M, sink);
+        float z = 0.f;
+        for (int s = lane; s < nsp; s += 32) {
+            const float *ml = A.part_ml + ((static_cast<int64_t>(t) * A.splits + s) * A.H + h) * 2;
+            const float w = ml[0] == -INFINITY ? 0.f : exp2f(ml[0] - Mall);
+            wgt[s] = w;
+            z += w * ml[1];
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        if (lane == 0) {
+            if (A.sinks) z += exp2f(sink - Mall);
+            inv_z = z > 0.f ? 1.f / z : 0.f;
+        }
+    }
+    __syncthreads();
+    const int d = threadIdx.x * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < nsp; ++s) {
+        const float w = wgt[s];
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+            A.part_o + ((static_cast<int64_t>(t) * A.splits + s) * A.H + h) * kHD + d));
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+    }
+    const float iz = inv_z;
+    *reinterpret_cast<float4 *>(o + d) = make_float4(acc.x * iz, acc.y * iz, acc.z * iz, acc.w * iz);
+    pdl_launch_dependents();
+}
+
+cudaError_t launch_gather(const Launch &lc, const RowSource &src, int32_t T, void *kv_buf,
+                          int32_t *kv_len, int32_t *status) {
+    if (T <= 0) return cudaSuccess;
+    const int rows = src.rows_per_token;
+    dim3 grid((rows + 7) / 8, T);
+    return launch_pdl(gather_kernel, grid, dim3(256), 0, lc.stream, src,
+                      static_cast<__nv_bfloat16 *>(kv_buf), kv_len, status);
+}
+
+cudaError_t launch_attention(const Launch &lc, const RowSource &src, int32_t T,
+                             const csa_params_t &p, const WsPlan &plan, const void *q,
+                             const float *sinks, float *out, float *part_o, float *part_ml,
+                             int32_t *status) {
+    if (T <= 0) return cudaSuccess;
+    AttnParams A;
+    A.R = src;
+    A.H = p.n_heads;
+    A.splits = plan.splits;
+    A.rows_split = plan.rows_split;
+    A.scale_log2 = p.scale * kLog2e;
+    A.q = static_cast<const __nv_bfloat16 *>(q);
+    A.sinks = sinks;
+    A.out = out;
+    A.part_o = part_o;
+    A.part_ml = part_ml;
+    A.status = status;
+    const size_t smem = sizeof(AttnSmem) + 128;
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid(plan.splits, p.n_heads / kHeadGroup, T);
+    e = launch_pdl(attention_kernel, grid, dim3(kAttnThreads), smem, lc.stream, A);
+    if (e != cudaSuccess || plan.splits == 1) return e;
+    return launch_pdl(combine_kernel, dim3(p.n_heads, T), dim3(128), 0, lc.stream, A);
+}
+
+}  // namespace csa

@@ -1,0 +1,111 @@
+// csa_internal.h -- host-side plumbing shared by the library's translation
+// units: workspace plan, launch context and the per-kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "csa.h"
+
+namespace csa {
+
+// Device-independent grid targets (sized for ~150-SM parts).
+constexpr int kTargetCtas = 296;
+constexpr int kAttnChunk = 32;   // rows per attention chunk (one online-softmax step)
+constexpr int kHeadGroup = 16;   // query heads per attention CTA
+
+struct WsPlan {
+    int64_t T = 0;
+    int64_t ld = 0;          // row stride of the workspace score matrix
+    int32_t top_k = 0;
+    int32_t H = 0;
+    int32_t cap = 0;         // candidate slots per token in the top-k filter
+    int32_t splits = 1;      // attention splits per token
+    int32_t rows_split = 0;  // rows per attention split (multiple of kAttnChunk)
+    // Layout: [per-token state | ... free ... | data].  The state slots sit at
+    // the front at offsets that depend only on the token index; the data
+    // regions are packed against the end of the caller's workspace, so no
+    // call's data ever lands on a state slot of a call with more tokens.
+    size_t state_bytes = 0;
+    size_t off_scores = 0, off_sel = 0, off_cand = 0;   // offsets inside the data area
+    size_t off_idx = 0, off_nsel = 0, off_part_o = 0, off_part_ml = 0;
+    size_t data_bytes = 0;
+    size_t total = 0;        // state + data + alignment slack
+};
+
+WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p);
+
+struct Launch {
+    cudaStream_t stream;
+    int sm_count;
+};
+
+// Top-k workspace pieces (device pointers).
+struct TopkWs {
+    uint32_t *state;  // [T][kStateWords]: histogram + counters, zero on entry and exit
+    int32_t *sel;     // [T][top_k]
+    uint64_t *cand;   // [T][cap]
+    int32_t cap;
+};
+
+// Where attention rows come from.
+struct RowSource {
+    int fused;                     // 0: gathered buffer, 1: indices + caches
+    const void *kv_buf;            // gathered: bf16 [T][rows_per_token][hd]
+    const int32_t *kv_len;         // gathered: [T]
+    int32_t rows_per_token;        // top_k + window
+    csa_layout_t L;                // fused
+    int32_t ratio, window, top_k;  // fused
+    const int32_t *idx;            // fused: [T][top_k]
+    const int32_t *n_sel;          // fused: [T]
+    const void *comp_kv;           // fused: bf16 [R][hd]
+};
+
+cudaError_t launch_indexer(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
+                           const void *q_idx, const float *w_idx, const void *k_idx,
+                           float *scores, int64_t ld, uint32_t *state, int32_t *status);
+
+// True when csa_decode's indexer can fold the pass-1 histogram of the top-k
+// into its epilogue (one token per indexer unit).
+bool indexer_fuses_hist(const csa_layout_t &L);
+
+cudaError_t launch_topk(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
+                        const float *scores, int64_t ld, const TopkWs &ws, bool hist_ready,
+                        int32_t *idx, int32_t *n_sel, int32_t *status);
+
+cudaError_t launch_gather(const Launch &lc, const RowSource &src, int32_t T, void *kv_buf,
+                          int32_t *kv_len, int32_t *status);
+
+cudaError_t launch_attention(const Launch &lc, const RowSource &src, int32_t T,
+                             const csa_params_t &p, const WsPlan &plan, const void *q,
+                             const float *sinks, float *out, float *part_o, float *part_ml,
+                             int32_t *status);
+
+// Launch helper: programmatic dependent launch on, so each kernel's prologue
+// may overlap the previous kernel's tail (kernels wait with griddepcontrol).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+CUresult encode_tensor_map_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
+                                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                                   uint32_t box_outer);
+
+}  // namespace csa

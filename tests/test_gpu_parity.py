@@ -1,0 +1,187 @@
+"""GPU parity: every C-ABI entry point against the CPU oracle on seeded inputs.
+
+Bars: indexer scores within relative 1e-4 of sum_h |w_h| ReLU(q_h.k) (plus an
+f32 floor); top-k bit-exact against the oracle's selection on the GPU's own
+scores; gather bit-exact; attention max-abs 2e-3 against the f64 oracle on the
+rows the GPU attended; the fused step bit-identical to the unfused chain's
+selection.
+"""
+import numpy as np
+import pytest
+import torch
+
+import csa_workloads as W
+import oracle
+from sparse_compressed_kv_gb300 import csa
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+def full_chain(run: H.Run, check_recall=True):
+    """Unfused chain with a parity check at every step, then the fused step."""
+    wl = run.wl
+    sc = run.scores()
+    H.check_scores(wl, sc)
+    idx, n_sel = run.topk(sc)
+    H.check_topk_exact(wl, sc, idx, n_sel)
+    kv_buf, kv_len = H.gpu_rows(run, idx, n_sel)
+    out = run.attention(kv_buf, kv_len)
+    err, cos = H.check_attention(wl, kv_buf, kv_len, out)
+    fout, fidx = run.decode()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(fidx.cpu().numpy(), idx.cpu().numpy())
+    # same rows, same kernel: the fused output equals the unfused one up to
+    # the order rows reach the kernel (identical here), so compare tightly
+    np.testing.assert_allclose(fout.cpu().numpy(), out.cpu().numpy(), rtol=0, atol=1e-6)
+    assert run.dev_status() == 0
+    rec = H.recall_vs_oracle(wl, idx, n_sel) if check_recall else None
+    return err, cos, rec
+
+
+def test_tiny(cuda_device):
+    err, cos, rec = full_chain(H.Run(W.tiny(), cuda_device))
+    assert cos > 0.9999 and rec >= 0.95
+
+
+def test_ragged_multi_sequence(cuda_device):
+    # three sequences, 1-2 tokens each; one short context (window clipped at 0),
+    # n_comp not a multiple of the 128-key tile
+    wl = W.make("ragged", seed=21, seq_lens=[4 * 300 + 3, 90, 4 * 1000 + 1], tokens=[1, 2, 1],
+                n_comp=[300, 22, 1000], top_k=64, n_heads=32, swa_cap=160)
+    full_chain(H.Run(wl, cuda_device))
+
+
+def test_grouped_tokens_single_sequence(cuda_device):
+    # one sequence, 37 tokens: the indexer groups 4 tokens per MMA (N = 256),
+    # the last group is partial; every token has its own causal cut
+    wl = W.make("chunk", seed=22, seq_lens=[4 * 700], tokens=[37], top_k=128, n_heads=16,
+                swa_cap=256)
+    full_chain(H.Run(wl, cuda_device))
+
+
+def test_topk_covers_everything_and_empty(cuda_device):
+    # token 0: position 2 -> no visible block (window only)
+    # token 1: top_k >= n_vis -> every visible block, attention is dense
+    wl = W.make("edges", seed=23, seq_lens=[2, 4 * 50 + 2], tokens=[1, 1], n_comp=[0, 50],
+                top_k=64, n_heads=16, swa_cap=128)
+    run = H.Run(wl, cuda_device)
+    full_chain(run, check_recall=False)
+    _, idx = run.decode()
+    idx = idx.cpu().numpy()
+    assert (idx[0] == -1).all()
+    assert list(idx[1, :50]) == list(range(50)) and (idx[1, 50:] == -1).all()
+
+
+def test_ties_resolve_to_lowest_index(cuda_device):
+    # duplicated keys give bit-identical scores: the cut falls inside a tie
+    wl = W.make("ties", seed=24, seq_lens=[4 * 2000], n_comp=[2000], top_k=100, n_heads=16)
+    base = wl.k_idx[:40].clone()
+    for rep in range(50):
+        wl.k_idx[40 * rep:40 * rep + 40] = base
+    run = H.Run(wl, cuda_device)
+    sc = run.scores()
+    idx, n_sel = run.topk(sc)
+    H.check_topk_exact(wl, sc, idx, n_sel)
+    assert run.dev_status() == 0
+
+
+def test_all_equal_scores_overflow_path(cuda_device):
+    # w = 0: every score is 0, every block ties, and the candidate list
+    # overflows its capacity: the resolver falls back to scanning the row
+    wl = W.make("flat", seed=25, seq_lens=[4 * 20000], n_comp=[20000], top_k=1000, n_heads=16)
+    wl.w_idx.zero_()
+    run = H.Run(wl, cuda_device)
+    sc = run.scores()
+    assert (sc.cpu()[0, :20000] == 0).all()
+    idx, n_sel = run.topk(sc)
+    assert list(idx.cpu().numpy()[0]) == list(range(1000))
+    H.check_topk_exact(wl, sc, idx, n_sel)
+
+
+def test_negative_and_signed_zero_scores(cuda_device):
+    wl = W.make("signs", seed=26, seq_lens=[4 * 3000], n_comp=[3000], top_k=300, n_heads=16)
+    wl.w_idx.copy_(-wl.w_idx.abs())        # every score <= 0, many exactly -0.0 or 0.0
+    run = H.Run(wl, cuda_device)
+    sc = run.scores()
+    idx, n_sel = run.topk(sc)
+    H.check_topk_exact(wl, sc, idx, n_sel)
+
+
+def test_determinism_and_workspace_reuse(cuda_device):
+    run = H.Run(W.make("det", seed=27, seq_lens=[4 * 5000], n_comp=[5000], top_k=256,
+                       n_heads=64), cuda_device)
+    o1, i1 = run.decode()
+    for _ in range(3):
+        o2, i2 = run.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2)
+    assert torch.equal(o1, o2)
+    assert run.dev_status() == 0
+
+
+def test_causality_perturbation(cuda_device):
+    wl = W.make("causal", seed=28, seq_lens=[4 * 600 + 1], n_comp=[600], comp_capacity=[700],
+                top_k=64, n_heads=16, swa_cap=256)
+    run = H.Run(wl, cuda_device)
+    o1, i1 = run.decode()
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(5)
+    wl.k_idx[600:] = W.bf16_normal(g, 100, wl.ihd) * 100
+    wl.comp_kv[600:] = W.bf16_normal(g, 100, wl.hd) * 100
+    p = int(wl.tok_pos[0])
+    inside = {x % wl.swa_cap for x in range(p - wl.window + 1, p + 1)}
+    for slot in range(wl.swa_cap):
+        if slot not in inside:
+            wl.swa_kv[0, slot] = W.bf16_normal(g, wl.hd) * 100
+    wl.comp_off[1] = 700       # the extra rows exist in the cache but are not visible
+    run2 = H.Run(wl, cuda_device)
+    o2, i2 = run2.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2) and torch.equal(o1, o2)
+
+
+def test_device_status_bits(cuda_device):
+    wl = W.make("status", seed=29, seq_lens=[4 * 100], n_comp=[100], top_k=8, n_heads=16)
+    run = H.Run(wl, cuda_device)
+    idx = torch.tensor([[0, 5, 150, -1, -1, -1, -1, -1]], dtype=torch.int32, device=cuda_device)
+    n_sel = torch.tensor([3], dtype=torch.int32, device=cuda_device)
+    kv_buf, kv_len = run.gather(idx, n_sel)
+    st = run.dev_status()
+    assert st & csa.DEV_BAD_INDEX
+    assert (kv_buf[0, 2].float() == 0).all()            # the bad row is zeroed, not clamped
+    np.testing.assert_array_equal(W.bits(kv_buf[0, 1]), W.bits(wl.comp_kv[5]))
+    # a window row the ring no longer holds
+    run.status.zero_()
+    run.d.swa_first_pos[0] = int(wl.tok_pos[0])          # only the current position resident
+    run.gather(torch.tensor([[0] + [-1] * 7], dtype=torch.int32, device=cuda_device),
+               torch.tensor([1], dtype=torch.int32, device=cuda_device))
+    assert run.dev_status() & csa.DEV_MISSING_SWA
+
+
+def test_sink_attention(cuda_device):
+    wl = W.tiny(seed=3)
+    run = H.Run(wl, cuda_device)
+    sc = run.scores()
+    idx, n_sel = run.topk(sc)
+    kv_buf, kv_len = run.gather(idx, n_sel)
+    sinks = torch.randn(wl.n_heads, generator=torch.Generator().manual_seed(4)).to(cuda_device)
+    out = run.attention(kv_buf, kv_len, sinks=sinks)
+    H.check_attention(wl, kv_buf, kv_len, out, sinks=sinks)
+    fout, _ = run.decode(sinks=sinks)
+    np.testing.assert_allclose(fout.cpu().numpy(), out.cpu().numpy(), rtol=0, atol=1e-6)
+
+
+def test_host_errors_on_gpu(cuda_device):
+    run = H.Run(W.tiny(), cuda_device)
+    small = torch.zeros(16, dtype=torch.uint8, device=cuda_device)
+    with pytest.raises(csa.CsaError) as e:
+        csa.csa_decode(run.layout, run.prm, run.d.q_idx, run.d.w_idx, run.d.k_idx,
+                       run.d.comp_kv, run.d.q, torch.empty(1, 16, 512, device=cuda_device),
+                       run.status, small)
+    assert e.value.code == 7   # CSA_ERR_WORKSPACE
+    bad = csa.params(16, 64, hd=256)
+    with pytest.raises(csa.CsaError) as e:
+        csa.csa_indexer_scores(run.layout, bad, run.d.q_idx, run.d.w_idx, run.d.k_idx,
+                               torch.empty(1, 256, device=cuda_device), run.status)
+    assert e.value.code == 2   # CSA_ERR_UNSUPPORTED
