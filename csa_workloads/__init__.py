@@ -260,4 +260,12 @@ def prefill(seed: int = 0, tokens: int = 4096, device=None) -> Workload:
                 n_comp=[last // 4], top_k=1024, n_heads=64, swa_cap=8192, device=device)
 
 
-NAMED = {"tiny": tiny, "64k": ctx64k, "1m": ctx1m, "batch32": batch32, "prefill": prefill}
+def hca1m(seed: int = 0, device=None) -> Workload:
+    """1M-context HCA layer: ratio 128, 8192 compressed rows (8 MiB), dense
+    attention over all of them plus the 128-row window, 64 heads."""
+    return make("hca1m", seed=seed, seq_lens=[1 << 20], tokens=[1], n_comp=[8192], top_k=1,
+                n_heads=64, swa_cap=128, ratio=128, device=device)
+
+
+NAMED = {"tiny": tiny, "64k": ctx64k, "1m": ctx1m, "batch32": batch32, "prefill": prefill,
+         "hca1m": hca1m}

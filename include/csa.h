@@ -114,12 +114,17 @@ int32_t csa_abi_version(void);
 
 /* Bytes of workspace `ws` that csa_topk, csa_sparse_mqa_decode and csa_decode
  * need for this layout and these params (one size serves all three).
- * The workspace must be zero-filled before its first use; each call that
- * completes without error leaves it zero-filled again, so it can be reused
- * by the next call on the same stream with no memset.  After a call that
- * returned an error or set a dev_status bit, zero it again.  Calls that may
- * run concurrently (different streams) need separate workspaces.
- * Returns CSA_ERR_INVALID_ARGUMENT / CSA_ERR_UNSUPPORTED on bad input. */
+ * The workspace is device memory, 256-byte aligned, owned by the caller.
+ * Its front holds per-token top-k state (8448 bytes per token) that must be
+ * zero when a call starts: zero-fill the workspace once after allocating it.
+ * Every call that completes without error leaves that state zero again, so
+ * the workspace is reused with no memset.  Scratch data is packed against
+ * the END of the buffer, so a workspace sized for the largest call (most
+ * tokens, most blocks) serves every smaller call as well.  After a call that
+ * returned an error or set a dev_status bit, zero the workspace again.
+ * Calls that may run concurrently (different streams) need separate
+ * workspaces.  Returns CSA_ERR_INVALID_ARGUMENT / CSA_ERR_UNSUPPORTED on bad
+ * input. */
 csa_status_t csa_workspace_size(const csa_layout_t *layout, const csa_params_t *params,
                                 size_t *bytes /* (host) out */);
 
@@ -127,8 +132,7 @@ csa_status_t csa_workspace_size(const csa_layout_t *layout, const csa_params_t *
  *   scores[t, s] = sum_h w_idx[t,h] * max(0, sum_d q_idx[t,h,d] * k_idx[comp_off[b]+s, d])
  * for s < n_vis(t); entries s >= n_vis(t) are not written.
  *   q_idx  bf16 [T, n_ih, ihd]     w_idx f32 [T, n_ih]
- *   k_idx  bf16 [R, ihd]           scores f32 [T, ld_scores], ld_scores >= max_comp_rows,
- *                                  ld_scores a multiple of 4.
+ *   k_idx  bf16 [R, ihd]           scores f32 [T, ld_scores], ld_scores >= max_comp_rows.
  * Products are exact (bf16 x bf16), sums are f32 (tensor-core accumulation
  * over d, then a fixed-order sum over h).  The result does not depend on the
  * stream, launch order or other tokens. */
@@ -189,6 +193,23 @@ csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params,
                         const void *comp_kv, const void *q, const float *sinks, float *out,
                         int32_t *idx_out, int32_t *dev_status, void *ws, size_t ws_bytes,
                         void *stream);
+
+/* Heavily compressed attention (HCA) decode ([Audit 1M], D4: HCA layers run
+ * no indexer and attend densely over every compressed entry; [Audit rewrite]
+ * PART 2: one entry per 128 tokens).  Token t attends every visible block
+ * 0 .. n_vis(t)-1 of its sequence (the same strictly-preceding rule, with
+ * params->ratio = 128 for HCA) in index order, then its window rows, with
+ * the same shared-KV attention as csa_sparse_mqa_decode; no selection and no
+ * gather buffer (rows are read in place).  params->top_k is not used.
+ *   comp_kv bf16 [R, hd], q bf16 [T, H, hd], sinks f32 [H] (nullable),
+ *   out f32 [T, H, hd].  Workspace: csa_hca_workspace_size bytes, same
+ *   contract as csa_workspace_size. */
+csa_status_t csa_hca_workspace_size(const csa_layout_t *layout, const csa_params_t *params,
+                                    size_t *bytes /* (host) out */);
+
+csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *params,
+                            const void *comp_kv, const void *q, const float *sinks, float *out,
+                            int32_t *dev_status, void *ws, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

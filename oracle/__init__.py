@@ -70,6 +70,9 @@ def _bind(lib):
     lib.csa_oracle_decode.argtypes = [i32, i32, p, p, p, i32, i32, i32, i32, i32, i32, i32, f64,
                                       p, p, p, p, p, i32, p, p, p, p, i64, p, p, p]
     lib.csa_oracle_decode.restype = i32
+    lib.csa_oracle_hca_decode.argtypes = [i32, i32, p, p, p, i32, i32, i32, i32, f64, p, p, i32,
+                                          p, p, p, p, p]
+    lib.csa_oracle_hca_decode.restype = i32
     return lib
 
 
@@ -227,6 +230,33 @@ class Oracle:
         return idx, n_sel, out
 
 
+def _hca_decode(self, comp_kv, swa_kv, q, tok_seq, tok_pos, comp_off, swa_first_pos,
+                window=128, ratio=128, scale=None, sinks=None):
+    """HCA step: out [T, H, hd] f64 and kv_len [T] (dense over visible blocks + window)."""
+    comp_kv = _c(comp_kv, np.uint16)
+    swa_kv = _c(swa_kv, np.uint16)
+    q = _c(q, np.uint16)
+    tok_seq = _c(tok_seq, np.int32)
+    tok_pos = _c(tok_pos, np.int64)
+    comp_off = _c(comp_off, np.int64)
+    swa_first_pos = _c(swa_first_pos, np.int64)
+    sinks = None if sinks is None else _c(sinks, np.float32)
+    T, H, hd = q.shape
+    B, swa_cap, _ = swa_kv.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(hd)
+    out = np.zeros((T, H, hd), dtype=np.float64)
+    kv_len = np.zeros(T, dtype=np.int32)
+    _check("hca_decode", self._lib.csa_oracle_hca_decode(
+        T, B, _ptr(tok_seq), _ptr(tok_pos), _ptr(comp_off), hd, H, window, ratio, float(scale),
+        _ptr(comp_kv), _ptr(swa_kv), swa_cap, _ptr(swa_first_pos), _ptr(q), _ptr(sinks),
+        _ptr(kv_len), _ptr(out)))
+    return out, kv_len
+
+
+Oracle.hca_decode = _hca_decode
+
+
 def default() -> Oracle:
     """The oracle built from csa_oracle.c (compiled on first use)."""
     global _default
@@ -275,3 +305,7 @@ def attention(*args, **kwargs):
 
 def decode(*args, **kwargs):
     return default().decode(*args, **kwargs)
+
+
+def hca_decode(*args, **kwargs):
+    return default().hca_decode(*args, **kwargs)

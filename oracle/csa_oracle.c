@@ -304,3 +304,49 @@ done:
     free(kv_len);
     return st;
 }
+
+/* ---- HCA: dense over every visible compressed row --------------------- */
+
+int32_t csa_oracle_hca_decode(int32_t T, int32_t num_seqs, const int32_t *tok_seq,
+                              const int64_t *tok_pos, const int64_t *comp_off, int32_t hd,
+                              int32_t H, int32_t window, int32_t ratio, double scale,
+                              const uint16_t *comp_kv, const uint16_t *swa_kv, int32_t swa_cap,
+                              const int64_t *swa_first_pos, const uint16_t *q,
+                              const float *sinks, int32_t *kv_len_out, double *out) {
+    if (T < 0 || window < 1 || ratio < 1) return CSA_ORACLE_EINVAL;
+    int64_t max_vis = 0;
+    for (int32_t t = 0; t < T; ++t) {
+        if (!check_token(t, num_seqs, tok_seq, tok_pos, comp_off)) return CSA_ORACLE_EINVAL;
+        int32_t b = tok_seq[t];
+        int64_t nv = csa_oracle_n_vis(comp_off[b + 1] - comp_off[b], tok_pos[t], ratio);
+        if (nv > max_vis) max_vis = nv;
+    }
+    /* every visible block is "selected": the mixed gather with idx = 0..n_vis-1 */
+    int32_t k_all = (int32_t)(max_vis > 0 ? max_vis : 1);
+    int64_t rows_per_token = (int64_t)k_all + window;
+    int32_t *idx = (int32_t *)malloc((size_t)(T > 0 ? T : 1) * (size_t)k_all * sizeof(int32_t));
+    int32_t *n_sel = (int32_t *)malloc((size_t)(T > 0 ? T : 1) * sizeof(int32_t));
+    int32_t *kv_len = (int32_t *)malloc((size_t)(T > 0 ? T : 1) * sizeof(int32_t));
+    uint16_t *kv_buf = (uint16_t *)malloc((size_t)(T > 0 ? T : 1) * (size_t)rows_per_token *
+                                          (size_t)hd * sizeof(uint16_t));
+    int32_t st = CSA_ORACLE_ENOMEM;
+    if (!idx || !n_sel || !kv_len || !kv_buf) goto done;
+    for (int32_t t = 0; t < T; ++t) {
+        int32_t b = tok_seq[t];
+        int64_t nv = csa_oracle_n_vis(comp_off[b + 1] - comp_off[b], tok_pos[t], ratio);
+        n_sel[t] = (int32_t)nv;
+        for (int32_t i = 0; i < k_all; ++i) idx[(int64_t)t * k_all + i] = i < nv ? i : -1;
+    }
+    st = csa_oracle_gather(T, hd, k_all, window, ratio, num_seqs, tok_seq, tok_pos, comp_off,
+                           idx, n_sel, comp_kv, swa_kv, swa_cap, swa_first_pos, kv_buf, kv_len);
+    if (st) goto done;
+    st = csa_oracle_attention(T, H, hd, rows_per_token, q, kv_buf, kv_len, scale, sinks, out);
+    if (!st && kv_len_out)
+        for (int32_t t = 0; t < T; ++t) kv_len_out[t] = kv_len[t];
+done:
+    free(idx);
+    free(n_sel);
+    free(kv_len);
+    free(kv_buf);
+    return st;
+}

@@ -110,6 +110,19 @@ int32_t csa_oracle_decode(int32_t T, int32_t num_seqs, const int32_t *tok_seq,
                           const float *sinks, double *scores_out, int64_t ld,
                           int32_t *idx_out, int32_t *n_sel_out, double *out);
 
+/* Heavily compressed attention (HCA) decode: no indexer and no selection;
+ * every visible compressed row (ratio blocks, typically 128 tokens each) in
+ * index order, then the window rows, then the same shared-KV attention.
+ * [Audit 1M], D4 ("HCA is dense over compressed entries") and [Audit
+ * rewrite] PART 2 (one HCA entry per 128 tokens).  n_vis follows the same
+ * strictly-preceding rule.  out [T, H, hd] double; kv_len_out [T] (nullable). */
+int32_t csa_oracle_hca_decode(int32_t T, int32_t num_seqs, const int32_t *tok_seq,
+                              const int64_t *tok_pos, const int64_t *comp_off, int32_t hd,
+                              int32_t H, int32_t window, int32_t ratio, double scale,
+                              const uint16_t *comp_kv, const uint16_t *swa_kv, int32_t swa_cap,
+                              const int64_t *swa_first_pos, const uint16_t *q,
+                              const float *sinks, int32_t *kv_len_out, double *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,8 @@ DEV_BAD_INDEX, DEV_MISSING_SWA, DEV_BAD_LAYOUT = 0x01, 0x02, 0x04
 DEV_CAPACITY, DEV_BAD_LENGTH, DEV_TIMEOUT = 0x08, 0x10, 0x20
 
 EXPORTS = ("csa_status_string", "csa_abi_version", "csa_workspace_size", "csa_indexer_scores",
-           "csa_topk", "csa_gather_mixed", "csa_sparse_mqa_decode", "csa_decode")
+           "csa_topk", "csa_gather_mixed", "csa_sparse_mqa_decode", "csa_decode",
+           "csa_hca_workspace_size", "csa_hca_decode")
 
 
 class CsaError(RuntimeError):
@@ -78,6 +79,8 @@ def load() -> ctypes.CDLL:
     lib.csa_gather_mixed.argtypes = [L, Pm, P, P, P, P, P, P, P]
     lib.csa_sparse_mqa_decode.argtypes = [i32, Pm, P, P, P, P, P, P, P, sz, P]
     lib.csa_decode.argtypes = [L, Pm, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.csa_hca_workspace_size.argtypes = [L, Pm, ctypes.POINTER(sz)]
+    lib.csa_hca_decode.argtypes = [L, Pm, P, P, P, P, P, P, sz, P]
     for fn in EXPORTS[2:]:
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
@@ -194,3 +197,24 @@ def csa_decode(layout: Layout, prm: csa_params_t, q_idx, w_idx, k_idx, comp_kv, 
         ctypes.byref(lc), ctypes.byref(prm), _p(q_idx), _p(w_idx), _p(k_idx), _p(comp_kv), _p(q),
         _p(sinks), _p(out), _p(idx_out), _p(dev_status), _p(ws), int(ws.numel()),
         _stream(stream)))
+
+
+def csa_hca_workspace_size(layout: Layout, prm: csa_params_t) -> int:
+    n = ctypes.c_size_t(0)
+    lc = layout.c()
+    _check("csa_hca_workspace_size", load().csa_hca_workspace_size(
+        ctypes.byref(lc), ctypes.byref(prm), ctypes.byref(n)))
+    return int(n.value)
+
+
+def hca_workspace(layout: Layout, prm: csa_params_t, device=None) -> torch.Tensor:
+    return torch.zeros(csa_hca_workspace_size(layout, prm), dtype=torch.uint8,
+                       device=device or layout.tok_seq.device)
+
+
+def csa_hca_decode(layout: Layout, prm: csa_params_t, comp_kv, q, out, dev_status, ws,
+                   sinks=None, stream=None):
+    lc = layout.c()
+    _check("csa_hca_decode", load().csa_hca_decode(
+        ctypes.byref(lc), ctypes.byref(prm), _p(comp_kv), _p(q), _p(sinks), _p(out),
+        _p(dev_status), _p(ws), int(ws.numel()), _stream(stream)))

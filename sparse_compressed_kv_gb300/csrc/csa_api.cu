@@ -14,7 +14,7 @@ namespace csa {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p) {
+WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_t rows_max_in) {
     WsPlan w;
     w.T = T;
     w.top_k = p.top_k;
@@ -22,7 +22,8 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p) {
     w.ld = ((max_comp_rows > 0 ? max_comp_rows : 1) + 3) / 4 * 4;
     w.cap = T <= 64 ? 8192 : 1024;
     // Attention split: enough CTAs for ~2 waves, at most 64 splits per token.
-    const int64_t rows_max = static_cast<int64_t>(p.top_k) + p.window;
+    const int64_t rows_max =
+        rows_max_in >= 0 ? rows_max_in : static_cast<int64_t>(p.top_k) + p.window;
     const int64_t chunks = (rows_max + kAttnChunk - 1) / kAttnChunk;
     const int64_t ctas = (T > 0 ? T : 1) * (p.n_heads / kHeadGroup);
     int64_t splits = (kTargetCtas + ctas - 1) / ctas;
@@ -243,7 +244,7 @@ csa_status_t csa_gather_mixed(const csa_layout_t *layout, const csa_params_t *pa
     CSA_TRY(current_device(&sms));
     Launch lc{static_cast<cudaStream_t>(stream), sms};
     RowSource R{};
-    R.fused = 1;
+    R.fused = kRowsSelected;
     R.rows_per_token = params->top_k + params->window;
     R.L = *layout;
     R.ratio = params->ratio;
@@ -270,7 +271,7 @@ csa_status_t csa_sparse_mqa_decode(int32_t num_tokens, const csa_params_t *param
     CSA_TRY(current_device(&sms));
     Launch lc{static_cast<cudaStream_t>(stream), sms};
     RowSource R{};
-    R.fused = 0;
+    R.fused = kRowsGathered;
     R.kv_buf = kv_buf;
     R.kv_len = kv_len;
     R.rows_per_token = params->top_k + params->window;
@@ -312,7 +313,7 @@ csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, 
     e = launch_topk(lc, *layout, *params, scores, plan.ld, tw, fuse, idx, nsel, dev_status);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     RowSource R{};
-    R.fused = 1;
+    R.fused = kRowsSelected;
     R.rows_per_token = params->top_k + params->window;
     R.L = *layout;
     R.ratio = params->ratio;
@@ -320,6 +321,49 @@ csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, 
     R.top_k = params->top_k;
     R.idx = idx;
     R.n_sel = nsel;
+    R.comp_kv = comp_kv;
+    return cuda_status(launch_attention(lc, R, layout->num_tokens, *params, plan, q, sinks, out,
+                                        reinterpret_cast<float *>(w + plan.off_part_o),
+                                        reinterpret_cast<float *>(w + plan.off_part_ml),
+                                        dev_status));
+}
+
+static int64_t hca_rows_max(const csa_layout_t *L, const csa_params_t *p) {
+    return (L->max_comp_rows > 0 ? L->max_comp_rows : 0) + p->window;
+}
+
+csa_status_t csa_hca_workspace_size(const csa_layout_t *layout, const csa_params_t *params,
+                                    size_t *bytes) {
+    if (!bytes || !layout) return CSA_ERR_INVALID_ARGUMENT;
+    CSA_TRY(check_params(params));
+    if (layout->num_tokens < 0 || layout->max_comp_rows < 0) return CSA_ERR_INVALID_ARGUMENT;
+    *bytes = make_plan(layout->num_tokens, 0, *params, hca_rows_max(layout, params)).total;
+    return CSA_OK;
+}
+
+csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *params,
+                            const void *comp_kv, const void *q, const float *sinks, float *out,
+                            int32_t *dev_status, void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, true));
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!q || !out || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (layout->total_comp_rows > 0 && !comp_kv) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(out) || (comp_kv && !aligned16(comp_kv)))
+        return CSA_ERR_INVALID_ARGUMENT;
+    const WsPlan plan = make_plan(layout->num_tokens, 0, *params, hca_rows_max(layout, params));
+    CSA_TRY(check_ws(plan, ws, ws_bytes));
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    uint8_t *w = data_base(ws, ws_bytes, plan);
+    RowSource R{};
+    R.fused = kRowsAllVisible;
+    R.rows_per_token = static_cast<int32_t>(hca_rows_max(layout, params));
+    R.L = *layout;
+    R.ratio = params->ratio;
+    R.window = params->window;
+    R.top_k = params->top_k;
     R.comp_kv = comp_kv;
     return cuda_status(launch_attention(lc, R, layout->num_tokens, *params, plan, q, sinks, out,
                                         reinterpret_cast<float *>(w + plan.off_part_o),

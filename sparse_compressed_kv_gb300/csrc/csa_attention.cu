@@ -45,7 +45,7 @@ __device__ __forceinline__ TokRows token_rows(const RowSource &R, int t) {
     r.off = 0;
     r.b = 0;
     r.bad = 0;
-    if (!R.fused) {
+    if (R.fused == kRowsGathered) {
         int32_t len = R.kv_len[t];
         if (len < 0 || len > R.rows_per_token) {
             r.bad = CSA_DEV_BAD_LENGTH;
@@ -60,10 +60,15 @@ __device__ __forceinline__ TokRows token_rows(const RowSource &R, int t) {
         r.len = 0;
         return r;
     }
-    int32_t ns = R.n_sel[t];
-    if (ns < 0 || ns > R.top_k) {
-        r.bad |= CSA_DEV_BAD_LENGTH;
-        ns = ns < 0 ? 0 : R.top_k;
+    int32_t ns;
+    if (R.fused == kRowsAllVisible) {
+        ns = static_cast<int32_t>(v.n_vis);   // every visible block, in index order
+    } else {
+        ns = R.n_sel[t];
+        if (ns < 0 || ns > R.top_k) {
+            r.bad |= CSA_DEV_BAD_LENGTH;
+            ns = ns < 0 ? 0 : R.top_k;
+        }
     }
     r.n_sel = ns;
     r.first = window_first(v.pos, R.window);
@@ -76,11 +81,12 @@ __device__ __forceinline__ TokRows token_rows(const RowSource &R, int t) {
 
 __device__ __forceinline__ const __nv_bfloat16 *row_ptr(const RowSource &R, const TokRows &tr,
                                                          int t, int j, int *bad) {
-    if (!R.fused)
+    if (R.fused == kRowsGathered)
         return static_cast<const __nv_bfloat16 *>(R.kv_buf) +
                (static_cast<int64_t>(t) * R.rows_per_token + j) * kHD;
     if (j < tr.n_sel) {
-        const int32_t s = R.idx[static_cast<int64_t>(t) * R.top_k + j];
+        const int32_t s =
+            R.fused == kRowsAllVisible ? j : R.idx[static_cast<int64_t>(t) * R.top_k + j];
         if (s < 0 || s >= tr.n_vis) {
             *bad |= CSA_DEV_BAD_INDEX;
             return nullptr;

@@ -37,7 +37,9 @@ struct WsPlan {
     size_t total = 0;        // state + data + alignment slack
 };
 
-WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p);
+// rows_max: most rows any token attends (top_k + window for CSA; for HCA,
+// every visible block + window); < 0 means top_k + window.
+WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_t rows_max = -1);
 
 struct Launch {
     cudaStream_t stream;
@@ -53,8 +55,11 @@ struct TopkWs {
 };
 
 // Where attention rows come from.
+enum RowMode { kRowsGathered = 0, kRowsSelected = 1, kRowsAllVisible = 2 };
+
 struct RowSource {
-    int fused;                     // 0: gathered buffer, 1: indices + caches
+    int fused;                     // RowMode: gathered buffer / selected indices / every
+                                   // visible block (HCA), the last two plus the window ring
     const void *kv_buf;            // gathered: bf16 [T][rows_per_token][hd]
     const int32_t *kv_len;         // gathered: [T]
     int32_t rows_per_token;        // top_k + window

@@ -26,6 +26,7 @@ namespace csa {
 
 constexpr int kSelThreads = 512;
 constexpr int kBitmapBits = 1 << 18;  // index window emitted per bitmap pass (32 KiB)
+constexpr int kStagedCand = kBitmapBits / 64;  // candidates that fit in the bitmap's space
 
 struct SelectParams {
     csa_layout_t L;
@@ -234,14 +235,22 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
         uint32_t need = kk - gt1;   // >= 1, all from digit-1 bin d1
         uint32_t prefix = d1;       // key bits fixed so far (top bits)
         int fixed = kD1Bits;        // how many top bits are fixed
-        // Candidate source: the compacted list, or the whole row on overflow.
+        // Candidate source: the compacted list staged in shared memory (it
+        // fits in the bitmap's space, which is only needed later), the list
+        // in global memory when it is longer, or the whole row on overflow.
         const int64_t m = overflow ? n : static_cast<int64_t>(ncand);
+        const bool staged = !overflow && ncand <= static_cast<uint32_t>(kStagedCand);
+        uint64_t *cs = reinterpret_cast<uint64_t *>(S.bitmap);
+        if (staged) {
+            for (uint32_t i = tid; i < ncand; i += blockDim.x) cs[i] = __ldcg(&candg[i]);
+            __syncthreads();
+        }
         auto cand_key = [&](int64_t i, uint32_t &key, int64_t &index) {
             if (overflow) {
                 key = score_key(__ldcg(&sc[i]));
                 index = i;
             } else {
-                const uint64_t c = __ldcg(&candg[i]);
+                const uint64_t c = staged ? cs[i] : __ldcg(&candg[i]);
                 key = static_cast<uint32_t>(c >> 32);
                 index = static_cast<int64_t>(c & 0xffffffffu);
             }

@@ -26,19 +26,20 @@ def bits_to_f64(b):
 class Run:
     """One workload on the GPU, with its layout, params and workspace."""
 
-    def __init__(self, wl: W.Workload, device):
+    def __init__(self, wl: W.Workload, device, max_comp_rows=None):
         self.wl = wl
         self.dev = device
         d = wl.to(device)
         self.d = d
+        mcr = max(1, wl.max_comp_rows if max_comp_rows is None else max_comp_rows)
         self.layout = csa.Layout(d.tok_seq, d.tok_pos, d.comp_off, d.swa_kv, d.swa_first_pos,
-                                 max_comp_rows=max(1, wl.max_comp_rows),
+                                 max_comp_rows=mcr,
                                  total_comp_rows=int(wl.k_idx.shape[0]), swa_cap=wl.swa_cap)
         self.prm = csa.params(wl.n_heads, wl.top_k, wl.window, wl.ratio, wl.scale)
         self.ws = csa.workspace(self.layout, self.prm)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.T = wl.num_tokens
-        self.ld = max(1, wl.max_comp_rows)
+        self.ld = mcr
 
     # -- oracle-side views
     def n_vis(self):

@@ -99,7 +99,8 @@ def test_prefill_chunk(cuda_device):
 def test_64k_decode_loop(cuda_device):
     wl = W.ctx64k()
     gen = torch.Generator().manual_seed(1234)
-    run = H.Run(wl, cuda_device)
+    # max_comp_rows is the cache capacity: one workspace serves the whole loop
+    run = H.Run(wl, cuda_device, max_comp_rows=int(wl.k_idx.shape[0]))
     for i in range(100):
         if i:
             W.ctx64k_step(wl, i, gen)
@@ -111,7 +112,6 @@ def test_64k_decode_loop(cuda_device):
             run.d.q_idx.copy_(wl.q_idx)
             run.d.w_idx.copy_(wl.w_idx)
             run.d.q.copy_(wl.q)
-            run.layout.max_comp_rows = wl.max_comp_rows
         out, fidx = run.decode()
         if i % 9 == 0 or i == 99:
             sc = run.scores()

@@ -57,6 +57,8 @@ MUTATIONS = [
     ("value is the previous row",
      "o[d] += p * csa_oracle_bf16_to_f64(rows[j * hd + d]);",
      "o[d] += p * csa_oracle_bf16_to_f64(rows[((j + L - 1) % L) * hd + d]);"),
+    ("HCA drops the newest visible block",
+     "n_sel[t] = (int32_t)nv;", "n_sel[t] = (int32_t)(nv > 0 ? nv - 1 : 0);"),
     ("sink added to the numerator side",
      "double zsink = sinks ? exp((double)sinks[h] - m) : 0.0;",
      "double zsink = sinks ? -0.5 * exp((double)sinks[h] - m) : 0.0;"),

@@ -394,6 +394,43 @@ def test_planted_blocks_are_selected():
     assert set(wl.planted.tolist()) <= set(idx[:n_sel].tolist())
 
 
+# ----------------------------------------------------------------------- HCA
+
+def test_hca_is_dense_attention_over_visible_rows_and_window():
+    """HCA (ratio 128): SDPA in float64 over every visible compressed row
+    (strictly preceding blocks) followed by the window rows."""
+    wl = W.make(seed=14, seq_lens=[128 * 40 + 5, 128 * 3 + 127, 60], tokens=[1, 2, 1],
+                n_comp=[40, 4, 0], ratio=128, window=16, swa_cap=24, hd=64, n_heads=4)
+    out, kv_len = oracle.hca_decode(W.bits(wl.comp_kv), W.bits(wl.swa_kv), W.bits(wl.q),
+                                    wl.tok_seq.numpy(), wl.tok_pos.numpy(), wl.comp_off.numpy(),
+                                    wl.swa_first_pos.numpy(), window=16, ratio=128)
+    for t in range(wl.num_tokens):
+        b = int(wl.tok_seq[t])
+        p = int(wl.tok_pos[t])
+        nv = min(int(wl.comp_off[b + 1] - wl.comp_off[b]), p // 128)
+        rows = _visible_rows(wl, t, nv)
+        assert kv_len[t] == len(rows)
+        q4 = torch.from_numpy(bits_to_f64(W.bits(wl.q)[t]))[None, :, None, :]
+        kv = torch.from_numpy(bits_to_f64(rows))[None, None].expand(1, 4, -1, -1)
+        ref = torch.nn.functional.scaled_dot_product_attention(q4, kv, kv, scale=wl.scale)
+        np.testing.assert_allclose(out[t], ref[0, :, 0].numpy(), rtol=1e-11, atol=1e-12)
+    # token 2 sits at 128*3+127 (p = 511): block 3 holds 384..511 and stays hidden
+    assert kv_len[1] == 3 + 16
+
+
+def test_hca_causality_perturbation():
+    wl = W.make(seed=15, seq_lens=[128 * 20 + 3], n_comp=[20], comp_capacity=[30], ratio=128,
+                window=8, swa_cap=16, hd=32, n_heads=2)
+    args = lambda w: (W.bits(w.comp_kv), W.bits(w.swa_kv), W.bits(w.q), w.tok_seq.numpy(),
+                      w.tok_pos.numpy(), w.comp_off.numpy(), w.swa_first_pos.numpy())
+    out0, _ = oracle.hca_decode(*args(wl), window=8, ratio=128)
+    g = torch.Generator().manual_seed(7)
+    wl.comp_kv[20:] = W.bf16_normal(g, 10, wl.hd) * 50
+    wl.comp_off[1] = 30
+    out1, _ = oracle.hca_decode(*args(wl), window=8, ratio=128)
+    np.testing.assert_array_equal(out0, out1)
+
+
 # --------------------------------------------------------------------- sizes
 
 def test_memory_sizing_matches_pages():
