@@ -167,16 +167,33 @@ def max_over_ranks(ms: float, device) -> float:
     return float(t.item())
 
 
+def capture(fn, stream):
+    """Capture fn() into a CUDA graph whose raw handle stays readable (torch
+    >= 2.9 keeps it only with keep_graph=True, then instantiates on demand)."""
+    try:
+        g, kept = torch.cuda.CUDAGraph(keep_graph=True), True
+    except TypeError:
+        g, kept = torch.cuda.CUDAGraph(), False
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    if kept:
+        g.instantiate()
+    return g
+
+
 def time_graphs(graphs, steps, warmup, stream):
-    for i in range(warmup):
-        graphs[i % len(graphs)].replay()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(steps):
-        graphs[(warmup + i) % len(graphs)].replay()
-    t1.record(stream)
+    """Replays go to torch's current stream, so make `stream` current: the
+    events then bracket exactly the `steps` replays."""
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(steps):
+            graphs[(warmup + i) % len(graphs)].replay()
+        t1.record(stream)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / steps
 
@@ -205,12 +222,7 @@ def run_ours(args, rank, world, device):
         for L in layers:
             step(L, stream)
     torch.cuda.synchronize()
-    graphs = []
-    for L in layers:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(L, stream)
-        graphs.append(g)
+    graphs = [capture(lambda L=L: step(L, stream), stream) for L in layers]
     per_step_launches = launches_in_graph(graphs[0])
 
     # ---- timed region: exactly `steps` decode steps
@@ -288,11 +300,7 @@ def run_ours(args, rank, world, device):
             for L in blayers:
                 bstep(L, stream)
         torch.cuda.synchronize()
-        for L in blayers:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                bstep(L, stream)
-            bgraphs.append(g)
+        bgraphs = [capture(lambda L=L: bstep(L, stream), stream) for L in blayers]
         bms = time_graphs(bgraphs, args.steps, args.warmup, stream)
         bab = sum(algorithmic_bytes(L.wl)["step"] for L in blayers) / len(blayers)
         batch = {"workload": "batch32: 32 sequences, contexts U{32K..128K}, one token each",
@@ -302,6 +310,42 @@ def run_ours(args, rank, world, device):
         torch.cuda.synchronize()
         if int(status.item()) != 0:
             raise RuntimeError("device status set in the batch32 region")
+
+    # ---- next row: HCA decode at 1M context (8192 compressed rows, dense)
+    hca = None
+    if not args.no_hca:
+        hl = [W.hca1m(seed=500 + i + 1000 * rank, device=device) for i in range(32)]
+        hd = []
+        for wl in hl:
+            d = wl.to(device)
+            lay = csa.Layout(d.tok_seq, d.tok_pos, d.comp_off, d.swa_kv, d.swa_first_pos,
+                             max_comp_rows=wl.max_comp_rows,
+                             total_comp_rows=int(wl.comp_kv.shape[0]), swa_cap=wl.swa_cap)
+            prm = csa.params(wl.n_heads, 1, wl.window, wl.ratio, wl.scale)
+            hd.append((wl, d, lay, prm, torch.empty(1, wl.n_heads, wl.hd, device=device)))
+        hws = csa.hca_workspace(hd[0][2], hd[0][3])
+
+        def hstep(x, s):
+            wl, d, lay, prm, out = x
+            csa.csa_hca_decode(lay, prm, d.comp_kv, d.q, out, status, hws, stream=s)
+        with torch.cuda.stream(stream):
+            for x in hd:
+                hstep(x, stream)
+        torch.cuda.synchronize()
+        hgraphs = [capture(lambda x=x: hstep(x, stream), stream) for x in hd]
+        hms = time_graphs(hgraphs, args.steps, args.warmup, stream)
+        hab = algorithmic_bytes(hl[0])
+        hbytes = (8192 + 128) * 1024 + 64 * 1024 + 64 * 2048
+        hca = {"workload": "hca1m: HCA decode, 1 token, ratio 128, 8192 compressed rows + 128 "
+                           "window rows, 64 heads, dense (32 rotating layers, 270 MB)",
+               "tokens_per_s_per_layer": round(world * 1e3 / hms, 1),
+               "ms_per_step": round(hms, 5), "algorithmic_bytes_per_step": hbytes,
+               "hbm_frac": round(hbytes / (hms * 1e-3) / 1e9 / hbm_peak, 4),
+               "launches_per_step": launches_in_graph(hgraphs[0])}
+        del hab
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("device status set in the HCA region")
 
     tok_s = world * 1e3 / ms
     achieved = ab["indexer"] / (idx_ms * 1e-3) / 1e9
@@ -330,6 +374,7 @@ def run_ours(args, rank, world, device):
         "e2e": e2e,
         "clocks": clk,
         "batch32": batch,
+        "hca": hca,
     }
     return line
 
@@ -440,6 +485,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-batch32", action="store_true")
+    ap.add_argument("--no-hca", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -156,7 +156,9 @@ struct AttnSmem {
     __nv_bfloat16 rows[2][kAttnChunk * kHD];        // 2 x 32 KiB, same swizzle
     const __nv_bfloat16 *ptr[2][kAttnChunk];
     float s[kHeadGroup][kAttnChunk];                // logits of the chunk (log2 units)
-    __nv_bfloat16 p[kHeadGroup][kAttnChunk + 8];    // probabilities, padded rows
+    // probabilities as two bf16 terms, p = hi + lo (padded rows): the PV product
+    // keeps ~16 bits of each weight instead of bf16's 8
+    __nv_bfloat16 p[2][kHeadGroup][kAttnChunk + 8];
     float m[kHeadGroup], l[kHeadGroup], alpha[kHeadGroup];
     TokRows tr;
 };
@@ -234,7 +236,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
     const uint32_t q_base = smem_addr(S.q);
-    const uint32_t p_base = smem_addr(&S.p[0][0]);
+    const uint32_t p_base = smem_addr(&S.p[0][0][0]);
+    constexpr uint32_t kPLoOffset = kHeadGroup * (kAttnChunk + 8) * 2;   // bytes from hi to lo
 
     for (int ci = 0; ci < nchunks; ++ci) {
         const int buf = ci & 1;
@@ -288,7 +291,9 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
             const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
-            S.p[h][lane] = __float2bfloat16_rn(p);
+            const __nv_bfloat16 p_hi = __float2bfloat16_rn(p);
+            S.p[0][h][lane] = p_hi;
+            S.p[1][h][lane] = __float2bfloat16_rn(p - __bfloat162float(p_hi));
             __syncwarp();
             if (lane == 0) {
                 S.l[h] = S.l[h] * alpha + sum;
@@ -310,10 +315,12 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
             }
 #pragma unroll
             for (int ks = 0; ks < kAttnChunk / 16; ++ks) {
-                uint32_t a0, a1, a2, a3;
+                uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
                 const int pr = (lane & 7) + ((lane >> 3) & 1) * 8;
                 const int pc = ks * 16 + (lane >> 4) * 8;
-                ldsm_x4(p_base + static_cast<uint32_t>((pr * (kAttnChunk + 8) + pc) * 2), a0, a1, a2, a3);
+                const uint32_t pa = p_base + static_cast<uint32_t>((pr * (kAttnChunk + 8) + pc) * 2);
+                ldsm_x4(pa, a0, a1, a2, a3);
+                ldsm_x4(pa + kPLoOffset, l0, l1, l2, l3);
                 const int vr = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
                 for (int np = 0; np < 8; ++np) {
@@ -322,6 +329,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
                     ldsm_x4_trans(rows_base + swz(vr, chunk), b0, b1, b2, b3);
                     mma_bf16_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
                     mma_bf16_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                    mma_bf16_16816(o[2 * np], l0, l1, l2, l3, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], l0, l1, l2, l3, b2, b3);
                 }
             }
         }
