@@ -211,6 +211,25 @@ csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *para
                             const void *comp_kv, const void *q, const float *sinks, float *out,
                             int32_t *dev_status, void *ws, size_t ws_bytes, void *stream);
 
+/* csa_topk without a workspace, for callers that cannot allocate device
+ * memory at all: an engine whose memory planner owns every byte of the GPU,
+ * or a plug-in that is not allowed to call the allocator, cannot hand
+ * csa_topk the workspace it needs.  The pages have no counterpart: this is a
+ * deployment convenience, not a step of the method.
+ *
+ * Same arguments, results and errors as csa_topk minus ws/ws_bytes.  The
+ * scratch is a fixed 1.25 MiB array inside libcsa.so, reserved on every GPU
+ * that loads the library until the process exits; it limits a call to at
+ * most 16 query tokens (more returns CSA_ERR_CAPACITY) and top_k <= 2048.
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up per device); make that first call before any stream capture.  Every
+ * call reuses the same array and clears the part that must start at zero, so
+ * calls that overlap on the GPU (two streams, two threads) race: serialise
+ * them. */
+csa_status_t csa_topk_noalloc(const csa_layout_t *layout, const csa_params_t *params,
+                              const float *scores, int64_t ld_scores, int32_t *idx,
+                              int32_t *n_sel, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
