@@ -115,7 +115,7 @@ int32_t csa_abi_version(void);
 /* Bytes of workspace `ws` that csa_topk, csa_sparse_mqa_decode and csa_decode
  * need for this layout and these params (one size serves all three).
  * The workspace is device memory, 256-byte aligned, owned by the caller.
- * Its front holds per-token top-k state (8448 bytes per token) that must be
+ * Its front holds per-token top-k state (16640 bytes per token) that must be
  * zero when a call starts: zero-fill the workspace once after allocating it.
  * Every call that completes without error leaves that state zero again, so
  * the workspace is reused with no memset.  Scratch data is packed against
@@ -218,9 +218,11 @@ csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *para
  * deployment convenience, not a step of the method.
  *
  * Same arguments, results and errors as csa_topk minus ws/ws_bytes.  The
- * scratch is a fixed 1.25 MiB array inside libcsa.so, reserved on every GPU
+ * scratch is a fixed 260 KiB array inside libcsa.so, reserved on every GPU
  * that loads the library until the process exits; it limits a call to at
  * most 16 query tokens (more returns CSA_ERR_CAPACITY) and top_k <= 2048.
+ * Each token's selection runs in one thread block here, so long rows take
+ * longer than with csa_topk.
  * The first call on a device looks up the array's device address (a one-time
  * set-up per device); make that first call before any stream capture.  Every
  * call reuses the same array and clears the part that must start at zero, so

@@ -20,7 +20,7 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     w.top_k = p.top_k;
     w.H = p.n_heads;
     w.ld = ((max_comp_rows > 0 ? max_comp_rows : 1) + 3) / 4 * 4;
-    w.cap = T <= 64 ? 8192 : 1024;
+    topk_grid(T, max_comp_rows, &w.topk_chunk, &w.topk_per_tok);
     // Attention split: enough CTAs for ~2 waves, at most 64 splits per token.
     const int64_t rows_max =
         rows_max_in >= 0 ? rows_max_in : static_cast<int64_t>(p.top_k) + p.window;
@@ -39,8 +39,9 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     w.state_bytes = Tz * kStateWords * 4;
     size_t off = 0;
     w.off_scores = off;  off = align_up(off + Tz * w.ld * 4, A);
-    w.off_sel = off;     off = align_up(off + Tz * p.top_k * 4, A);
-    w.off_cand = off;    off = align_up(off + Tz * w.cap * 8, A);
+    w.off_slots = off;
+    if (w.topk_per_tok > 1) off = align_up(off + Tz * w.topk_per_tok * w.topk_chunk * 8, A);
+    w.off_slot_cnt = off; off = align_up(off + Tz * w.topk_per_tok * 4, A);
     w.off_idx = off;     off = align_up(off + Tz * p.top_k * 4, A);
     w.off_nsel = off;    off = align_up(off + Tz * 4, A);
     w.off_part_o = off;
@@ -225,8 +226,8 @@ csa_status_t csa_topk(const csa_layout_t *layout, const csa_params_t *params, co
     CSA_TRY(current_device(&sms));
     Launch lc{static_cast<cudaStream_t>(stream), sms};
     uint8_t *w = data_base(ws, ws_bytes, plan);
-    TopkWs tw{static_cast<uint32_t *>(ws), reinterpret_cast<int32_t *>(w + plan.off_sel),
-              reinterpret_cast<uint64_t *>(w + plan.off_cand), plan.cap};
+    TopkWs tw{static_cast<uint32_t *>(ws), reinterpret_cast<uint64_t *>(w + plan.off_slots),
+              reinterpret_cast<uint32_t *>(w + plan.off_slot_cnt)};
     return cuda_status(launch_topk(lc, *layout, *params, scores, ld_scores, tw, false, idx, n_sel,
                                    dev_status));
 }
@@ -308,8 +309,8 @@ csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, 
     cudaError_t e = launch_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores, plan.ld,
                                    fuse ? state : nullptr, dev_status);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
-    TopkWs tw{state, reinterpret_cast<int32_t *>(w + plan.off_sel),
-              reinterpret_cast<uint64_t *>(w + plan.off_cand), plan.cap};
+    TopkWs tw{state, reinterpret_cast<uint64_t *>(w + plan.off_slots),
+              reinterpret_cast<uint32_t *>(w + plan.off_slot_cnt)};
     e = launch_topk(lc, *layout, *params, scores, plan.ld, tw, fuse, idx, nsel, dev_status);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     RowSource R{};
@@ -325,7 +326,7 @@ csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, 
     return cuda_status(launch_attention(lc, R, layout->num_tokens, *params, plan, q, sinks, out,
                                         reinterpret_cast<float *>(w + plan.off_part_o),
                                         reinterpret_cast<float *>(w + plan.off_part_ml),
-                                        dev_status));
+                                        dev_status, true));
 }
 
 static int64_t hca_rows_max(const csa_layout_t *L, const csa_params_t *p) {

@@ -25,6 +25,7 @@ namespace csa {
 constexpr int kAttnThreads = 128;
 constexpr int kRowBytes = kHD * 2;  // 1 KiB
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxSplits = 64;   // attention splits per token (the plan never exceeds it)
 
 // Row count of token t and the address of its row j (nullptr: skipped row).
 struct TokRows {
@@ -108,6 +109,7 @@ __device__ __forceinline__ const __nv_bfloat16 *row_ptr(const RowSource &R, cons
 __global__ void __launch_bounds__(256) gather_kernel(const RowSource R, __nv_bfloat16 *kv_buf,
                                                      int32_t *kv_len, int32_t *status) {
     pdl_wait();
+    pdl_launch_dependents();
     const int t = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = blockIdx.x * 8 + warp;
@@ -132,7 +134,6 @@ __global__ void __launch_bounds__(256) gather_kernel(const RowSource R, __nv_bfl
             if (lane == 0) raise_status(status, bad);
         }
     }
-    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------- attention
@@ -149,6 +150,9 @@ struct AttnParams {
     float *part_o;           // [T][splits][H][512]
     float *part_ml;          // [T][splits][H][2]  (m in log2 units, l)
     int32_t *status;
+    int32_t early_q;         // q may be read before the grid-dependency wait: the
+                             // launching chain's first kernel already waited on
+                             // whatever produced the caller's inputs
 };
 
 struct AttnSmem {
@@ -169,22 +173,29 @@ __device__ __forceinline__ uint32_t swz(int r, int chunk) {
     return static_cast<uint32_t>(r * kRowBytes + ((chunk ^ (r & 7)) << 4));
 }
 
+// 32 x 64 sixteen-byte copies of the chunk whose row addresses are in S.ptr[buf]
+// (null rows are zero-filled and masked later).
+__device__ __forceinline__ void issue_chunk_copies(AttnSmem &S, const RowSource &R, int buf) {
+    uint8_t *base = reinterpret_cast<uint8_t *>(S.rows[buf]);
+    const void *dummy = R.comp_kv ? R.comp_kv : R.kv_buf;
+    for (int i = threadIdx.x; i < kAttnChunk * 64; i += kAttnThreads) {
+        const int r = i >> 6, c = i & 63;
+        const __nv_bfloat16 *src = S.ptr[buf][r];
+        cp_async16(base + swz(r, c), src ? static_cast<const void *>(src + c * 8) : dummy,
+                   src != nullptr);
+    }
+    cp_async_commit();
+}
+
+// Row addresses of the chunk starting at r0 (warp 0), then its copies.
 __device__ __forceinline__ void issue_chunk(AttnSmem &S, const RowSource &R, int t, int buf,
                                             int r0, int r_end, int *bad) {
-    // pointers of the 32 rows (warp 0), then 32 x 64 16-byte copies (all threads)
     if (threadIdx.x < kAttnChunk) {
         const int j = r0 + threadIdx.x;
         S.ptr[buf][threadIdx.x] = j < r_end ? row_ptr(R, S.tr, t, j, bad) : nullptr;
     }
     __syncthreads();
-    uint8_t *base = reinterpret_cast<uint8_t *>(S.rows[buf]);
-    for (int i = threadIdx.x; i < kAttnChunk * 64; i += kAttnThreads) {
-        const int r = i >> 6, c = i & 63;
-        const __nv_bfloat16 *src = S.ptr[buf][r];
-        cp_async16(base + swz(r, c), src ? static_cast<const void *>(src + c * 8) : R.comp_kv ? R.comp_kv : R.kv_buf,
-                   src != nullptr);
-    }
-    cp_async_commit();
+    issue_chunk_copies(S, R, buf);
 }
 
 __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParams A) {
@@ -195,41 +206,53 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
 
-    pdl_wait();
-    if (threadIdx.x == 0) S.tr = token_rows(A.R, t);
-    __syncthreads();
-    const int len = S.tr.len;
-    const int r_begin = split * A.rows_split;
-    const int r_end = min(len, r_begin + A.rows_split);
-    int bad = (threadIdx.x == 0 && split == 0 && hg == 0) ? S.tr.bad : 0;
-
-    if (r_begin >= r_end) {
-        // nothing here; with one split this CTA still owns the output (zeros)
-        if (A.splits == 1) {
-            float *o = A.out + (static_cast<int64_t>(t) * A.H + hg * kHeadGroup) * kHD;
-            for (int i = threadIdx.x; i < kHeadGroup * kHD; i += kAttnThreads) o[i] = 0.f;
-        }
-        raise_status(A.status, bad);
-        pdl_launch_dependents();
-        return;
-    }
-
-    // q of this head group
-    {
-        const __nv_bfloat16 *qg = A.q + (static_cast<int64_t>(t) * A.H + hg * kHeadGroup) * kHD;
+    const int h0 = hg * kHeadGroup;
+    auto load_q = [&]() {
+        const __nv_bfloat16 *qg = A.q + (static_cast<int64_t>(t) * A.H + h0) * kHD;
         uint8_t *qs = reinterpret_cast<uint8_t *>(S.q);
         for (int i = threadIdx.x; i < kHeadGroup * 64; i += kAttnThreads) {
             const int r = i >> 6, ch = i & 63;
             cp_async16(qs + swz(r, ch), qg + r * kHD + ch * 8, true);
         }
         cp_async_commit();
+    };
+    if (A.early_q) load_q();
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // Warp 0 resolves the token's rows and the first chunk's row addresses in
+    // one pass (every lane reads the same token record: a broadcast).
+    const int r_begin = split * A.rows_split;
+    int bad = 0;
+    if (warp == 0) {
+        const TokRows tr = token_rows(A.R, t);
+        if (lane == 0) S.tr = tr;
+        const int re = min(tr.len, r_begin + A.rows_split);
+        const int j = r_begin + lane;
+        S.ptr[0][lane] = j < re ? row_ptr(A.R, tr, t, j, &bad) : nullptr;
+        if (lane == 0 && split == 0 && hg == 0) bad |= tr.bad;
     }
+    __syncthreads();
+    const int len = S.tr.len;
+    const int r_end = min(len, r_begin + A.rows_split);
+
+    if (r_begin >= r_end) {
+        if (A.early_q) cp_async_wait<0>();
+        // nothing here; with one split this CTA still owns the output (zeros)
+        if (A.splits == 1) {
+            float *o = A.out + (static_cast<int64_t>(t) * A.H + h0) * kHD;
+            for (int i = threadIdx.x; i < kHeadGroup * kHD; i += kAttnThreads) o[i] = 0.f;
+        }
+        raise_status(A.status, bad);
+        return;
+    }
+    if (!A.early_q) load_q();
     if (threadIdx.x < kHeadGroup) {
         S.m[threadIdx.x] = -INFINITY;
         S.l[threadIdx.x] = 0.f;
     }
     const int nchunks = (r_end - r_begin + kAttnChunk - 1) / kAttnChunk;
-    issue_chunk(S, A.R, t, 0, r_begin, r_end, &bad);
+    issue_chunk_copies(S, A.R, 0);
 
     float o[16][4];
 #pragma unroll
@@ -253,18 +276,22 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
 
         // ---- logits: warp w owns rows 8w..8w+7 of the chunk, all 16 heads
         {
+            // two independent accumulation chains (even / odd k-steps)
             float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            float sacc2[4] = {0.f, 0.f, 0.f, 0.f};
             const int rr = warp * 8 + (lane & 7);
+            const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll 4
             for (int kk = 0; kk < kHD / 16; kk += 2) {
-                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                uint32_t a0, a1, a2, a3, e0, e1, e2, e3, b0, b1, b2, b3;
                 ldsm_x4(q_base + swz(qr, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+                ldsm_x4(q_base + swz(qr, (kk + 1) * 2 + (lane >> 4)), e0, e1, e2, e3);
                 ldsm_x4(rows_base + swz(rr, kk * 2 + (lane >> 3)), b0, b1, b2, b3);
                 mma_bf16_16816(sacc, a0, a1, a2, a3, b0, b1);
-                ldsm_x4(q_base + swz(qr, (kk + 1) * 2 + (lane >> 4)), a0, a1, a2, a3);
-                mma_bf16_16816(sacc, a0, a1, a2, a3, b2, b3);
+                mma_bf16_16816(sacc2, e0, e1, e2, e3, b2, b3);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];
             // c-fragment: heads g, g+8; rows 2c, 2c+1 of this warp's 8
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -338,7 +365,6 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
     }
 
     // ---- write
-    const int h0 = hg * kHeadGroup;
     if (A.splits == 1) {
         float z0 = S.l[g], z1 = S.l[g + 8];
         if (A.sinks) {
@@ -368,12 +394,12 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
         }
     }
     raise_status(A.status, bad);
-    pdl_launch_dependents();
 }
 
 // out[t,h,:] = sum_s 2^(m_s - M) O_s / (sum_s 2^(m_s - M) l_s [+ 2^(sink*log2e - M)])
-__global__ void __launch_bounds__(128) combine_kernel(const AttnParams A) {
+__global__ void __launch_bounds__(256) combine_kernel(const AttnParams A) {
     pdl_wait();
+    pdl_launch_dependents();
     const int h = blockIdx.x, t = blockIdx.y;
     __shared__ float wgt[64];
     __shared__ float inv_z;
@@ -382,25 +408,43 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams A) {
     float *o = A.out + (static_cast<int64_t>(t) * A.H + h) * kHD;
     if (nsp <= 0) {
         for (int i = threadIdx.x; i < kHD; i += blockDim.x) o[i] = 0.f;
-        pdl_launch_dependents();
         return;
     }
+    // Issue every partial load first (they do not depend on the weights),
+    // then the (m, l) of each split, then combine: one round trip.
+    const int d = threadIdx.x * 2;   // 256 threads x 2 columns
+    const float *pb = A.part_o + (static_cast<int64_t>(t) * A.splits * A.H + h) * kHD + d;
+    const int64_t pstride = static_cast<int64_t>(A.H) * kHD;
+    float2 v[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+        if (s < nsp) v[s] = __ldcg(reinterpret_cast<const float2 *>(pb + s * pstride));
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        float M = -INFINITY;
-        for (int s = lane; s < nsp; s += 32)
-            M = fmaxf(M, A.part_ml[((static_cast<int64_t>(t) * A.splits + s) * A.H + h) * 2]);
+        // each lane holds (m, l) of splits lane and lane + 32 (at most 64 splits)
+        float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+        const float *mlb = A.part_ml + (static_cast<int64_t>(t) * A.splits * A.H + h) * 2;
+        const int64_t stride = static_cast<int64_t>(A.H) * 2;
+        if (lane < nsp) {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(mlb + lane * stride));
+            m0 = x.x;
+            l0 = x.y;
+        }
+        if (lane + 32 < nsp) {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(mlb + (lane + 32) * stride));
+            m1 = x.x;
+            l1 = x.y;
+        }
+        float M = fmaxf(m0, m1);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         const float sink = A.sinks ? A.sinks[h] * kLog2e : -INFINITY;
         const float Mall = fmaxf(M, sink);
-        float z = 0.f;
-        for (int s = lane; s < nsp; s += 32) {
-            const float *ml = A.part_ml + ((static_cast<int64_t>(t) * A.splits + s) * A.H + h) * 2;
-            const float w = ml[0] == -INFINITY ? 0.f : exp2f(ml[0] - Mall);
-            wgt[s] = w;
-            z += w * ml[1];
-        }
+        const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - Mall);
+        const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - Mall);
+        if (lane < nsp) wgt[lane] = w0;
+        if (lane + 32 < nsp) wgt[lane + 32] = w1;
+        float z = w0 * l0 + w1 * l1;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         if (lane == 0) {
@@ -409,20 +453,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams A) {
         }
     }
     __syncthreads();
-    const int d = threadIdx.x * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nsp; ++s) {
-        const float w = wgt[s];
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-            A.part_o + ((static_cast<int64_t>(t) * A.splits + s) * A.H + h) * kHD + d));
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+        if (s < nsp) {
+            const float w = wgt[s];
+            acc.x += w * v[s].x;
+            acc.y += w * v[s].y;
+        }
     }
     const float iz = inv_z;
-    *reinterpret_cast<float4 *>(o + d) = make_float4(acc.x * iz, acc.y * iz, acc.z * iz, acc.w * iz);
-    pdl_launch_dependents();
+    *reinterpret_cast<float2 *>(o + d) = make_float2(acc.x * iz, acc.y * iz);
 }
 
 cudaError_t launch_gather(const Launch &lc, const RowSource &src, int32_t T, void *kv_buf,
@@ -430,6 +471,8 @@ cudaError_t launch_gather(const Launch &lc, const RowSource &src, int32_t T, voi
     if (T <= 0) return cudaSuccess;
     const int rows = src.rows_per_token;
     dim3 grid((rows + 7) / 8, T);
+    cudaError_t e = set_kernel_smem(gather_kernel, 0);
+    if (e != cudaSuccess) return e;
     return launch_pdl(gather_kernel, grid, dim3(256), 0, lc.stream, src,
                       static_cast<__nv_bfloat16 *>(kv_buf), kv_len, status);
 }
@@ -437,7 +480,7 @@ cudaError_t launch_gather(const Launch &lc, const RowSource &src, int32_t T, voi
 cudaError_t launch_attention(const Launch &lc, const RowSource &src, int32_t T,
                              const csa_params_t &p, const WsPlan &plan, const void *q,
                              const float *sinks, float *out, float *part_o, float *part_ml,
-                             int32_t *status) {
+                             int32_t *status, bool early_q) {
     if (T <= 0) return cudaSuccess;
     AttnParams A;
     A.R = src;
@@ -451,15 +494,16 @@ cudaError_t launch_attention(const Launch &lc, const RowSource &src, int32_t T,
     A.part_o = part_o;
     A.part_ml = part_ml;
     A.status = status;
+    A.early_q = early_q ? 1 : 0;
     const size_t smem = sizeof(AttnSmem) + 128;
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_kernel_smem(attention_kernel, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.splits, p.n_heads / kHeadGroup, T);
     e = launch_pdl(attention_kernel, grid, dim3(kAttnThreads), smem, lc.stream, A);
     if (e != cudaSuccess || plan.splits == 1) return e;
-    return launch_pdl(combine_kernel, dim3(p.n_heads, T), dim3(128), 0, lc.stream, A);
+    e = set_kernel_smem(combine_kernel, 0);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(combine_kernel, dim3(p.n_heads, T), dim3(256), 0, lc.stream, A);
 }
 
 }  // namespace csa

@@ -28,10 +28,11 @@ constexpr int kD2Bins = 1 << kD2Bits;
 constexpr int kD2Shift = kD1Shift - kD2Bits;  // 10
 constexpr int kD3Bins = 1 << kD2Shift;        // 1024
 
-// Per-token top-k state at the front of the workspace: the digit-1 histogram
-// followed by the counters, kStateWords 32-bit words per token.  It must be
-// zero when a call starts; the kernel that consumes it zeroes it again.
-constexpr int kStateWords = kD1Bins + 64;  // 8448 bytes, a multiple of 256
+// Per-token top-k state at the front of the workspace: the digit-1 and
+// digit-2 histograms followed by the counters, kStateWords 32-bit words per
+// token.  It must be zero when a call starts; the kernel that consumes it
+// zeroes it again.
+constexpr int kStateWords = kD1Bins + kD2Bins + 64;  // 16640 bytes, a multiple of 256
 
 struct TokCounters {
     uint32_t sel;     // entries appended to the "certainly selected" list

@@ -313,7 +313,13 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-bool indexer_fuses_hist(const csa_layout_t &L) { return !(L.num_seqs == 1 && L.num_tokens >= 4); }
+bool indexer_fuses_hist(const csa_layout_t &L) {
+    // one token per unit, and a top-k that filters with several CTAs per token
+    if (L.num_seqs == 1 && L.num_tokens >= 4) return false;
+    int32_t chunk = 0, per_tok = 0;
+    topk_grid(L.num_tokens, L.max_comp_rows, &chunk, &per_tok);
+    return per_tok > 1;
+}
 
 template <int G, bool kHist>
 static cudaError_t launch_g(const Launch &lc, const CUtensorMap &tk, const CUtensorMap &tq,
@@ -321,8 +327,7 @@ static cudaError_t launch_g(const Launch &lc, const CUtensorMap &tk, const CUten
     using C = IdxCfg<G>;
     const size_t smem = C::smem_bytes(kHist);
     auto kern = indexer_kernel<G, kHist>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_kernel_smem(kern, smem);
     if (e != cudaSuccess) return e;
     int64_t grid = tiles_bound < lc.sm_count ? tiles_bound : lc.sm_count;
     if (grid < 1) grid = 1;

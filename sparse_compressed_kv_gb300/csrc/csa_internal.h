@@ -17,13 +17,16 @@ namespace csa {
 constexpr int kTargetCtas = 296;
 constexpr int kAttnChunk = 32;   // rows per attention chunk (one online-softmax step)
 constexpr int kHeadGroup = 16;   // query heads per attention CTA
+constexpr int kMaxFilterChunk = 4096;  // scores per top-k filter CTA (multi-CTA mode)
+constexpr int kMaxPerTok = 512;        // top-k filter CTAs per token
 
 struct WsPlan {
     int64_t T = 0;
     int64_t ld = 0;          // row stride of the workspace score matrix
     int32_t top_k = 0;
     int32_t H = 0;
-    int32_t cap = 0;         // candidate slots per token in the top-k filter
+    int32_t topk_chunk = 0;  // scores per top-k filter CTA
+    int32_t topk_per_tok = 1;  // top-k filter CTAs per token (1: one CTA owns the row)
     int32_t splits = 1;      // attention splits per token
     int32_t rows_split = 0;  // rows per attention split (multiple of kAttnChunk)
     // Layout: [per-token state | ... free ... | data].  The state slots sit at
@@ -31,7 +34,7 @@ struct WsPlan {
     // regions are packed against the end of the caller's workspace, so no
     // call's data ever lands on a state slot of a call with more tokens.
     size_t state_bytes = 0;
-    size_t off_scores = 0, off_sel = 0, off_cand = 0;   // offsets inside the data area
+    size_t off_scores = 0, off_slots = 0, off_slot_cnt = 0;   // offsets inside the data area
     size_t off_idx = 0, off_nsel = 0, off_part_o = 0, off_part_ml = 0;
     size_t data_bytes = 0;
     size_t total = 0;        // state + data + alignment slack
@@ -46,13 +49,16 @@ struct Launch {
     int sm_count;
 };
 
-// Top-k workspace pieces (device pointers).
+// Top-k workspace pieces (device pointers).  With slots == nullptr the top-k
+// runs one CTA per token and needs only the state.
 struct TopkWs {
-    uint32_t *state;  // [T][kStateWords]: histogram + counters, zero on entry and exit
-    int32_t *sel;     // [T][top_k]
-    uint64_t *cand;   // [T][cap]
-    int32_t cap;
+    uint32_t *state;     // [T][kStateWords]: histogram + counters, zero on entry and exit
+    uint64_t *slots;     // [T][per_tok][chunk] filter output (multi-CTA mode)
+    uint32_t *slot_cnt;  // [T][per_tok]
 };
+
+// Shape of the top-k filter grid for T tokens of at most max_comp_rows blocks.
+void topk_grid(int64_t T, int64_t max_comp_rows, int32_t *chunk, int32_t *per_tok);
 
 // Where attention rows come from.
 enum RowMode { kRowsGathered = 0, kRowsSelected = 1, kRowsAllVisible = 2 };
@@ -88,7 +94,7 @@ cudaError_t launch_gather(const Launch &lc, const RowSource &src, int32_t T, voi
 cudaError_t launch_attention(const Launch &lc, const RowSource &src, int32_t T,
                              const csa_params_t &p, const WsPlan &plan, const void *q,
                              const float *sinks, float *out, float *part_o, float *part_ml,
-                             int32_t *status);
+                             int32_t *status, bool early_q = false);
 
 // Launch helper: programmatic dependent launch on, so each kernel's prologue
 // may overlap the previous kernel's tail (kernels wait with griddepcontrol).
@@ -106,6 +112,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Dynamic shared memory limit, and the largest shared-memory carveout for
+// every kernel of the library: all kernels then run under one L1/shared
+// split, so an SM never has to drain and reconfigure between them.
+template <typename K>
+cudaError_t set_kernel_smem(K kernel, size_t dyn_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) return e;
+    if (dyn_bytes > 48 * 1024)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(dyn_bytes));
+    return e;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).

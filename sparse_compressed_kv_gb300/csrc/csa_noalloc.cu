@@ -13,15 +13,13 @@
 
 namespace csa {
 
-// Limits of the no-allocation top-k (the scratch is sized for them):
+// Limits of the no-allocation top-k (the scratch is sized for them): the
+// top-k runs one CTA per token here, which needs only each token's state
+// (histogram and counters), kStateWords words per token.
 constexpr int kNoAllocMaxTokens = 16;
-constexpr int kNoAllocCap = 8192;  // candidate slots per token
-constexpr size_t kNoAllocStateBytes = size_t(kNoAllocMaxTokens) * kStateWords * 4;
-constexpr size_t kNoAllocSelBytes = size_t(kNoAllocMaxTokens) * kMaxTopK * 4;
-constexpr size_t kNoAllocCandBytes = size_t(kNoAllocMaxTokens) * kNoAllocCap * 8;
-constexpr size_t kNoAllocBytes = kNoAllocStateBytes + kNoAllocSelBytes + kNoAllocCandBytes;
+constexpr size_t kNoAllocBytes = size_t(kNoAllocMaxTokens) * kStateWords * 4;
 
-// 135,168 + 131,072 + 1,048,576 bytes = 1.25 MiB per device.
+// 16 x 16640 bytes = 260 KiB per device.
 static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocBytes];
 
 // Device address of g_topk_scratch, looked up once per device.  In host code
@@ -78,9 +76,7 @@ extern "C" csa_status_t csa_topk_noalloc(const csa_layout_t *layout, const csa_p
     // whatever the previous call (or an interrupted one) left, so clear them.
     const size_t state = size_t(layout->num_tokens) * kStateWords * 4;
     if (cudaMemsetAsync(b, 0, state, s) != cudaSuccess) return CSA_ERR_CUDA;
-    TopkWs tw{reinterpret_cast<uint32_t *>(b), reinterpret_cast<int32_t *>(b + kNoAllocStateBytes),
-              reinterpret_cast<uint64_t *>(b + kNoAllocStateBytes + kNoAllocSelBytes),
-              kNoAllocCap};
+    TopkWs tw{reinterpret_cast<uint32_t *>(b), nullptr, nullptr};
     Launch lc{s, sms};
     return launch_topk(lc, *layout, *params, scores, ld_scores, tw, false, idx, n_sel,
                        dev_status) == cudaSuccess

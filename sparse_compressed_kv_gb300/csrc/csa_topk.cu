@@ -7,26 +7,30 @@
 // Output: the k' = min(top_k, n_vis) selected blocks in ascending index.
 //
 // Radix select on the order-preserving 32-bit key of each score:
-//   digit 1 = key[31:21]  histogram built by the indexer epilogue (csa_decode)
-//                          or by score_hist_kernel (csa_topk);
-//   filter (many CTAs per token): blocks whose digit 1 exceeds the threshold
-//                          digit are certainly selected; blocks equal to it are
-//                          candidates;
-//   resolve (the last CTA of each token, by atomic ticket): digits 2 and 3
-//                          over the candidates give the exact k-th key; ties at
+//   digit 1 = key[31:21]  histogram built by the indexer epilogue (csa_decode),
+//                          by score_hist_kernel (csa_topk), or, with one CTA
+//                          per token, by that CTA itself;
+//   filter                 every CTA of a token finds the threshold digit d1
+//                          and compacts, with a block-wide scan, the entries
+//                          (key, index) whose digit 1 is >= d1 into its own
+//                          output slot: no shared counters, no contention;
+//   resolve                the last CTA of the token (atomic ticket) stages
+//                          every slot's entries in shared memory in one round
+//                          trip; digit-1 winners are in, digits 2 and 3 over
+//                          the threshold bin give the exact k-th key; ties at
 //                          that key are taken in ascending index order; a
 //                          bitmap over the index range emits the set sorted.
-// The result is a pure function of the score bits: no step depends on the
-// order in which CTAs or atomics run.  The kernel that consumes a counter
-// resets it, so the workspace is left zeroed for the next call.
+// The result is a pure function of the score bits.  The kernel that consumes
+// the per-token state (histogram, ticket) zeroes it for the next call.
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
 namespace csa {
 
 constexpr int kSelThreads = 512;
-constexpr int kBitmapBits = 1 << 18;  // index window emitted per bitmap pass (32 KiB)
-constexpr int kStagedCand = kBitmapBits / 64;  // candidates that fit in the bitmap's space
+constexpr int kStageCap = 8192;        // entries staged in shared memory (64 KiB)
+static_assert(kStageCap % (kSelThreads / 32) == 0, "per-warp staging runs");
+constexpr int kMaxPerThread = kMaxFilterChunk / kSelThreads;
 
 struct SelectParams {
     csa_layout_t L;
@@ -35,10 +39,10 @@ struct SelectParams {
     const float *scores;
     int64_t ld;
     uint32_t *state;      // [T][kStateWords]: digit-1 histogram, then TokCounters
-    int32_t *sel;         // [T][top_k]
-    uint64_t *cand;       // [T][cap]
-    int32_t cap;
+    uint64_t *slots;      // [T][per_tok][chunk] (key << 32 | index), multi-CTA mode
+    uint32_t *slot_cnt;   // [T][per_tok]
     int32_t chunk;        // scores per filter CTA
+    int32_t per_tok;      // filter CTAs per token
     int32_t local_hist;   // one CTA per token builds digit 1 itself
     int32_t *idx_out;     // [T][top_k]
     int32_t *nsel_out;    // [T]
@@ -47,7 +51,7 @@ struct SelectParams {
 
 // ---------------------------------------------------------------- helpers
 
-// Block-wide exclusive scan of one value per thread (kSelThreads threads).
+// Block-wide exclusive scan of one value per thread.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_tmp,
                                                     uint32_t *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -100,23 +104,14 @@ __device__ void find_threshold_digit(const uint32_t *h, int nbins, uint32_t k, u
     __syncthreads();
 }
 
-__device__ __forceinline__ void warp_append(bool pred, uint32_t *counter, uint32_t limit,
-                                            int32_t *buf_i32, uint64_t *buf_u64, uint64_t val,
-                                            int32_t ival) {
-    const unsigned m = __ballot_sync(0xffffffffu, pred);
-    if (!m) return;
+// Shared-memory histogram increment, aggregated over the lanes of a warp that
+// hit the same bin (scores cluster in few bins: plain atomics would serialise).
+__device__ __forceinline__ void smem_hist_add(uint32_t *h, uint32_t bin, bool active) {
+    const unsigned act = __ballot_sync(0xffffffffu, active);
+    if (!active) return;
+    const unsigned peers = __match_any_sync(act, bin);
     const int lane = threadIdx.x & 31;
-    const int leader = __ffs(m) - 1;
-    uint32_t base = 0;
-    if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(m)));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    if (pred) {
-        const uint32_t pos = base + __popc(m & ((1u << lane) - 1u));
-        if (pos < limit) {
-            if (buf_i32) buf_i32[pos] = ival;
-            else buf_u64[pos] = val;
-        }
-    }
+    if (lane == __ffs(peers) - 1) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(peers)));
 }
 
 // ---------------------------------------------------------------- digit-1 histogram
@@ -124,6 +119,7 @@ __device__ __forceinline__ void warp_append(bool pred, uint32_t *counter, uint32
 __global__ void __launch_bounds__(256) score_hist_kernel(const SelectParams P) {
     __shared__ uint32_t h[kD1Bins];
     pdl_wait();
+    pdl_launch_dependents();
     const int t = blockIdx.y;
     for (int i = threadIdx.x; i < kD1Bins; i += blockDim.x) h[i] = 0;
     __syncthreads();
@@ -132,234 +128,325 @@ __global__ void __launch_bounds__(256) score_hist_kernel(const SelectParams P) {
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * P.chunk;
     const int64_t b1 = min(n, b0 + P.chunk);
     const float *sc = P.scores + static_cast<int64_t>(t) * P.ld;
-    for (int64_t i = b0 + threadIdx.x; i < b1; i += blockDim.x)
-        atomicAdd(&h[score_key(sc[i]) >> kD1Shift], 1u);
+    for (int64_t base = b0; base < b1; base += blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        smem_hist_add(h, i < b1 ? score_key(sc[i]) >> kD1Shift : 0u, i < b1);
+    }
     __syncthreads();
     uint32_t *gh = P.state + static_cast<int64_t>(t) * kStateWords;
     for (int i = threadIdx.x; i < kD1Bins; i += blockDim.x)
         if (h[i]) atomicAdd(&gh[i], h[i]);
-    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------- filter + resolve
 
 struct SelectSmem {
-    uint32_t h[kD1Bins];          // digit histograms (reused per pass)
+    uint32_t h[kD1Bins];           // digit-1 histogram, then digit-3 histogram
+    uint32_t h2[kD2Bins];          // digit-2 histogram of the threshold bin
     uint32_t warp_tmp[32];
-    uint32_t bitmap[kBitmapBits / 32];
-    int32_t sel[kMaxTopK];        // selected indices (unordered until emitted)
-    uint32_t nsel;
-    int32_t d;                    // threshold digit of the current pass
-    uint32_t gt;                  // count strictly above the threshold digit
+    uint64_t stage[kStageCap];     // entries (key << 32 | index), ascending index
+    uint32_t prefix[kMaxPerTok + 1];
+    uint32_t wcount[32];           // one-CTA mode: entries per warp range
+    uint32_t nstage;
+    uint32_t overflow;
+    int32_t d;                     // threshold digit of the current pass
+    uint32_t gt;                   // count strictly above the threshold digit
     uint32_t total;
     uint32_t last;
-    uint32_t tie_taken;
 };
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams P) {
     extern __shared__ uint8_t smem_raw[];
-    SelectSmem &S = *reinterpret_cast<SelectSmem *>(smem_raw);
+    SelectSmem &S = *reinterpret_cast<SelectSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
     const int t = blockIdx.y;
     const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    constexpr int kWarps = kSelThreads / 32;
 
     pdl_wait();
+    pdl_launch_dependents();
 
+    uint32_t *gh = P.state + static_cast<int64_t>(t) * kStateWords;   // digit-1 histogram
+    uint32_t *gh2 = gh + kD1Bins;                                       // digit-2 histogram
+    TokCounters *cnt = reinterpret_cast<TokCounters *>(gh2 + kD2Bins);
+    // the histogram's address depends only on t: load it while the token's
+    // layout is being read
+    uint32_t hreg[kD1Bins / kSelThreads];
+    if (!P.local_hist)
+#pragma unroll
+        for (int u = 0; u < kD1Bins / kSelThreads; ++u) hreg[u] = __ldcg(&gh[u * kSelThreads + tid]);
     const TokenView v = token_view(P.L, P.ratio, t);
     if (v.bad && blockIdx.x == 0 && tid == 0) raise_status(P.status, v.bad);
     const int64_t n = v.n_vis;
     const uint32_t kk = static_cast<uint32_t>(min(static_cast<int64_t>(P.top_k), n));
     const float *sc = P.scores + static_cast<int64_t>(t) * P.ld;
-    uint32_t *gh = P.state + static_cast<int64_t>(t) * kStateWords;
-    TokCounters *cnt = reinterpret_cast<TokCounters *>(gh + kD1Bins);
+    const bool rank = kk > 0 && kk < n;
 
-    // ---- digit-1 histogram and threshold (every CTA of the token)
-    if (kk > 0 && kk < n) {
+    // ---- digit-1 threshold (every CTA of the token) and this CTA's entries
+    if (rank) {
         if (P.local_hist) {
             for (int i = tid; i < kD1Bins; i += blockDim.x) S.h[i] = 0;
+            for (int i = tid; i < kD2Bins; i += blockDim.x) S.h2[i] = 0;
             __syncthreads();
-            for (int64_t i = tid; i < n; i += blockDim.x) atomicAdd(&S.h[score_key(sc[i]) >> kD1Shift], 1u);
+            // every lane runs the same number of iterations: the warp-wide
+            // collectives inside smem_hist_add need the whole warp
+            for (int64_t base = 0; base < n; base += blockDim.x) {
+                const int64_t i = base + tid;
+                smem_hist_add(S.h, i < n ? score_key(__ldcg(&sc[i])) >> kD1Shift : 0u, i < n);
+            }
         } else {
-            for (int i = tid; i < kD1Bins; i += blockDim.x) S.h[i] = __ldcg(&gh[i]);
+#pragma unroll
+            for (int u = 0; u < kD1Bins / kSelThreads; ++u) S.h[u * kSelThreads + tid] = hreg[u];
         }
         __syncthreads();
         find_threshold_digit(S.h, kD1Bins, kk, S.warp_tmp, &S.d, &S.gt);
         const uint32_t d1 = static_cast<uint32_t>(S.d);
 
-        // ---- filter this CTA's slice of the index range
-        const int64_t b0 = P.local_hist ? 0 : static_cast<int64_t>(blockIdx.x) * P.chunk;
-        const int64_t b1 = P.local_hist ? n : min(n, b0 + P.chunk);
-        int32_t *selg = P.sel + static_cast<int64_t>(t) * P.top_k;
-        uint64_t *candg = P.cand + static_cast<int64_t>(t) * P.cap;
-        for (int64_t base = b0; base < b1; base += blockDim.x) {
-            const int64_t i = base + tid;
-            uint32_t key = 0, dg = 0;
-            const bool in = i < b1;
-            if (in) {
-                key = score_key(__ldcg(&sc[i]));
-                dg = key >> kD1Shift;
+        if (P.local_hist) {
+            // One CTA owns the row.  Warp w compacts its contiguous index range
+            // in order into its own part of the staging area (ballot + popc),
+            // and histograms digit 2 of the threshold bin.
+            constexpr int kPerWarpCap = kStageCap / kWarps;
+            const int64_t span = (n + kWarps - 1) / kWarps;
+            const int64_t w0 = min(n, static_cast<int64_t>(warp) * span);
+            const int64_t w1 = min(n, w0 + span);
+            uint32_t cntw = 0;
+            uint64_t *buf = S.stage + warp * kPerWarpCap;
+            for (int64_t base = w0; base < w1; base += 32) {
+                const int64_t i = base + lane;
+                uint32_t key = 0;
+                if (i < w1) key = score_key(__ldcg(&sc[i]));
+                const uint32_t dg = key >> kD1Shift;
+                const bool keep = i < w1 && dg >= d1;
+                const unsigned m = __ballot_sync(0xffffffffu, keep);
+                const uint32_t p = cntw + __popc(m & ((1u << lane) - 1u));
+                if (keep && p < static_cast<uint32_t>(kPerWarpCap))
+                    buf[p] = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(i);
+                smem_hist_add(S.h2, (key >> kD2Shift) & (kD2Bins - 1), i < w1 && dg == d1);
+                cntw += __popc(m);
             }
-            warp_append(in && dg > d1, &cnt->sel, static_cast<uint32_t>(P.top_k), selg, nullptr, 0,
-                        static_cast<int32_t>(i));
-            warp_append(in && dg == d1, &cnt->cand, static_cast<uint32_t>(P.cap), nullptr, candg,
-                        (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(i), 0);
+            if (lane == 0) S.wcount[warp] = cntw;
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t tot = 0, of = 0;
+                for (int w = 0; w < kWarps; ++w) {
+                    of |= S.wcount[w] > static_cast<uint32_t>(kPerWarpCap);
+                    S.prefix[w] = tot;
+                    tot += S.wcount[w];
+                }
+                S.nstage = tot;
+                S.overflow = of;
+            }
+            __syncthreads();
+            if (!S.overflow) {
+                // pack the per-warp runs into one ascending list (in place: each
+                // run moves to a lower or equal offset, processed warp by warp)
+                for (int w = 1; w < kWarps; ++w) {
+                    const uint32_t c = S.wcount[w];
+                    uint64_t v0 = 0;
+                    for (uint32_t j0 = 0; j0 < c; j0 += blockDim.x) {
+                        const uint32_t j = j0 + tid;
+                        if (j < c) v0 = S.stage[w * kPerWarpCap + j];
+                        __syncthreads();
+                        if (j < c) S.stage[S.prefix[w] + j] = v0;
+                        __syncthreads();
+                    }
+                }
+            }
+        } else {
+            // This CTA's slice: thread-contiguous runs kept in registers, so the
+            // block-wide scan writes the entries in ascending index order.
+            const int64_t b0 = static_cast<int64_t>(blockIdx.x) * P.chunk;
+            const int64_t b1 = min(n, b0 + P.chunk);
+            const int64_t my0 = b0 + static_cast<int64_t>(tid) * kMaxPerThread;
+            uint32_t keys[kMaxPerThread];
+            uint32_t mine = 0;
+#pragma unroll
+            for (int e = 0; e < kMaxPerThread; ++e) {
+                const int64_t i = my0 + e;
+                keys[e] = i < b1 ? score_key(__ldcg(&sc[i])) : 0u;
+                const uint32_t dg = keys[e] >> kD1Shift;
+                mine += (i < b1 && dg >= d1) ? 1u : 0u;
+                if (i < b1 && dg == d1) atomicAdd(&gh2[(keys[e] >> kD2Shift) & (kD2Bins - 1)], 1u);
+            }
+            uint32_t pos = block_excl_scan(mine, S.warp_tmp, &S.total);
+            uint64_t *slot = P.slots + (static_cast<int64_t>(t) * P.per_tok + blockIdx.x) * P.chunk;
+#pragma unroll
+            for (int e = 0; e < kMaxPerThread; ++e) {
+                const int64_t i = my0 + e;
+                if (i < b1 && (keys[e] >> kD1Shift) >= d1)
+                    slot[pos++] = (static_cast<uint64_t>(keys[e]) << 32) | static_cast<uint32_t>(i);
+            }
+            if (tid == 0) P.slot_cnt[static_cast<int64_t>(t) * P.per_tok + blockIdx.x] = S.total;
         }
     }
 
-    // ---- last CTA of this token resolves
-    __syncthreads();
-    if (tid == 0) {
+    // ---- the last CTA of this token resolves
+    if (!P.local_hist) {
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            const uint32_t prev = atomicAdd(&cnt->ticket, 1u);
+            S.last = (prev == gridDim.x - 1) ? 1u : 0u;
+        }
+        __syncthreads();
+        if (!S.last) return;
         __threadfence();
-        const uint32_t prev = atomicAdd(&cnt->ticket, 1u);
-        S.last = (prev == gridDim.x - 1) ? 1u : 0u;
     }
-    __syncthreads();
-    if (!S.last) {
-        pdl_launch_dependents();
-        return;
-    }
-    __threadfence();
 
     int32_t *out = P.idx_out + static_cast<int64_t>(t) * P.top_k;
-    if (kk == 0 || kk == n) {
+    if (!rank) {
         // nothing to rank: none visible, or every visible block fits
         for (int i = tid; i < P.top_k; i += blockDim.x) out[i] = i < static_cast<int>(kk) ? i : -1;
     } else {
         const uint32_t d1 = static_cast<uint32_t>(S.d);
-        const uint32_t gt1 = S.gt;
-        const uint32_t ncand = __ldcg(&cnt->cand);
-        const bool overflow = ncand > static_cast<uint32_t>(P.cap);
-        const int32_t *selg = P.sel + static_cast<int64_t>(t) * P.top_k;
-        const uint64_t *candg = P.cand + static_cast<int64_t>(t) * P.cap;
-        for (uint32_t i = tid; i < gt1; i += blockDim.x) S.sel[i] = __ldcg(&selg[i]);
-        if (tid == 0) S.nsel = gt1;
-        uint32_t need = kk - gt1;   // >= 1, all from digit-1 bin d1
-        uint32_t prefix = d1;       // key bits fixed so far (top bits)
-        int fixed = kD1Bits;        // how many top bits are fixed
-        // Candidate source: the compacted list staged in shared memory (it
-        // fits in the bitmap's space, which is only needed later), the list
-        // in global memory when it is longer, or the whole row on overflow.
-        const int64_t m = overflow ? n : static_cast<int64_t>(ncand);
-        const bool staged = !overflow && ncand <= static_cast<uint32_t>(kStagedCand);
-        uint64_t *cs = reinterpret_cast<uint64_t *>(S.bitmap);
-        if (staged) {
-            for (uint32_t i = tid; i < ncand; i += blockDim.x) cs[i] = __ldcg(&candg[i]);
-            __syncthreads();
-        }
-        auto cand_key = [&](int64_t i, uint32_t &key, int64_t &index) {
-            if (overflow) {
-                key = score_key(__ldcg(&sc[i]));
-                index = i;
-            } else {
-                const uint64_t c = staged ? cs[i] : __ldcg(&candg[i]);
-                key = static_cast<uint32_t>(c >> 32);
-                index = static_cast<int64_t>(c & 0xffffffffu);
-            }
-        };
-        // ---- digits 2 and 3 among keys matching the fixed prefix
-        for (int pass = 0; pass < 2; ++pass) {
-            const int bits = pass == 0 ? kD2Bits : kD2Shift;
-            const int shift = 32 - fixed - bits;
-            const uint32_t mask = (1u << bits) - 1u;
-            for (int i = tid; i < kD1Bins; i += blockDim.x) S.h[i] = 0;
-            __syncthreads();
-            for (int64_t i = tid; i < m; i += blockDim.x) {
-                uint32_t key;
-                int64_t index;
-                cand_key(i, key, index);
-                if ((key >> (32 - fixed)) == prefix) atomicAdd(&S.h[(key >> shift) & mask], 1u);
+        uint32_t need = kk - S.gt;   // >= 1, all from digit-1 bin d1
+        if (!P.local_hist) {
+            // slot counts and the digit-2 histogram in one round trip
+            const int pt = P.per_tok;
+            const uint32_t c = tid < pt ? __ldcg(&P.slot_cnt[static_cast<int64_t>(t) * pt + tid]) : 0u;
+#pragma unroll
+            for (int u = 0; u < kD2Bins / kSelThreads; ++u)
+                S.h2[u * kSelThreads + tid] = __ldcg(&gh2[u * kSelThreads + tid]);
+            const uint32_t off = block_excl_scan(c, S.warp_tmp, &S.total);
+            if (tid < pt) S.prefix[tid] = off;
+            if (tid == 0) {
+                S.prefix[pt] = S.total;
+                S.nstage = S.total;
+                S.overflow = S.total > static_cast<uint32_t>(kStageCap);
             }
             __syncthreads();
-            find_threshold_digit(S.h, kD1Bins, need, S.warp_tmp, &S.d, &S.gt);
-            need -= S.gt;
-            prefix = (prefix << bits) | static_cast<uint32_t>(S.d);
-            fixed += bits;
-        }
-        // prefix is now the full k-th key tau; need = how many keys equal to tau are taken
-        const uint32_t tau = prefix;
-        const uint32_t eq = S.h[S.d];
-        // every key > tau among the candidates is selected
-        for (int64_t base = 0; base < m; base += blockDim.x) {
-            const int64_t i = base + tid;
-            uint32_t key = 0;
-            int64_t index = 0;
-            if (i < m) cand_key(i, key, index);
-            const bool take = i < m && (key >> (32 - kD1Bits)) == d1 && (key > tau || (key == tau && need == eq));
-            const unsigned bm = __ballot_sync(0xffffffffu, take);
-            if (bm) {
-                const int lane = tid & 31;
-                const int leader = __ffs(bm) - 1;
-                uint32_t pos = 0;
-                if (lane == leader) pos = atomicAdd(&S.nsel, static_cast<uint32_t>(__popc(bm)));
-                pos = __shfl_sync(0xffffffffu, pos, leader);
-                if (take) {
-                    const uint32_t q = pos + __popc(bm & ((1u << lane) - 1u));
-                    if (q < static_cast<uint32_t>(kMaxTopK)) S.sel[q] = static_cast<int32_t>(index);
+            if (!S.overflow) {
+                // addresses first (binary search over the slot prefix), then
+                // eight independent loads in flight per thread
+                const uint64_t *base = P.slots + static_cast<int64_t>(t) * pt * P.chunk;
+                const uint32_t ns = S.nstage;
+                for (uint32_t e0 = 0; e0 < ns; e0 += 8 * blockDim.x) {
+                    uint64_t val[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t e = e0 + u * blockDim.x + tid;
+                        int lo = 0, hi = pt;  // prefix[lo] <= e < prefix[hi]
+                        while (hi - lo > 1) {
+                            const int mid = (lo + hi) >> 1;
+                            if (S.prefix[mid] <= e) lo = mid;
+                            else hi = mid;
+                        }
+                        val[u] = e < ns ? __ldcg(&base[static_cast<int64_t>(lo) * P.chunk +
+                                                      (e - S.prefix[lo])])
+                                        : 0ull;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t e = e0 + u * blockDim.x + tid;
+                        if (e < ns) S.stage[e] = val[u];
+                    }
                 }
             }
         }
         __syncthreads();
-        if (need != eq) {
-            // ties straddle the cut: take the `need` lowest indices with key == tau,
-            // scanning the row in index order.
-            if (tid == 0) S.tie_taken = 0;
-            __syncthreads();
-            for (int64_t base = 0; base < n; base += blockDim.x) {
-                const int64_t i = base + tid;
-                const bool hit = i < n && score_key(__ldcg(&sc[i])) == tau;
-                const uint32_t before = block_excl_scan(hit ? 1u : 0u, S.warp_tmp, &S.total);
-                const uint32_t taken = S.tie_taken;
-                if (hit && taken + before < need) S.sel[S.nsel + taken + before] = static_cast<int32_t>(i);
-                __syncthreads();
-                if (tid == 0) S.tie_taken = taken + S.total;
-                __syncthreads();
-                if (S.tie_taken >= need) break;
+        // Entries in ascending index order: the staged list, or, when it did
+        // not fit, the whole row filtered by digit 1.
+        const bool staged = !S.overflow;
+        const int64_t m = staged ? static_cast<int64_t>(S.nstage) : n;
+        auto entry = [&](int64_t i, uint32_t &key, int64_t &index) {
+            if (staged) {
+                const uint64_t c = S.stage[i];
+                key = static_cast<uint32_t>(c >> 32);
+                index = static_cast<int64_t>(c & 0xffffffffu);
+            } else {
+                key = score_key(__ldcg(&sc[i]));
+                index = i;
             }
-            if (tid == 0) S.nsel += need;
-            __syncthreads();
+        };
+        // ---- digit 2 from its histogram, then digit 3 over the few entries
+        // that share digits 1 and 2
+        find_threshold_digit(S.h2, kD2Bins, need, S.warp_tmp, &S.d, &S.gt);
+        need -= S.gt;
+        const uint32_t pre22 = (d1 << kD2Bits) | static_cast<uint32_t>(S.d);
+        for (int i = tid; i < kD1Bins; i += blockDim.x) S.h[i] = 0;
+        __syncthreads();
+        for (int64_t base = 0; base < m; base += blockDim.x) {
+            const int64_t i = base + tid;
+            uint32_t key = 0;
+            int64_t index;
+            if (i < m) entry(i, key, index);
+            smem_hist_add(S.h, key & (kD3Bins - 1), i < m && (key >> kD2Shift) == pre22);
         }
-        // ---- emit in ascending index through a bitmap of the index range
-        const uint32_t ns = S.nsel;  // == kk
-        uint32_t written = 0;
-        for (int64_t w0 = 0; w0 < n; w0 += kBitmapBits) {
-            const int64_t wlen = min(static_cast<int64_t>(kBitmapBits), n - w0);
-            const int nwords = static_cast<int>((wlen + 31) >> 5);
-            for (int i = tid; i < nwords; i += blockDim.x) S.bitmap[i] = 0;
-            __syncthreads();
-            for (uint32_t i = tid; i < ns; i += blockDim.x) {
-                const int64_t x = S.sel[i];
-                if (x >= w0 && x < w0 + wlen) atomicOr(&S.bitmap[(x - w0) >> 5], 1u << ((x - w0) & 31));
+        __syncthreads();
+        find_threshold_digit(S.h, kD1Bins, need, S.warp_tmp, &S.d, &S.gt);
+        need -= S.gt;
+        const uint32_t tau = (pre22 << kD2Shift) | static_cast<uint32_t>(S.d);
+        const uint32_t eq = S.h[S.d];
+        // ---- ordered compaction: every key above tau, then the `need`
+        // lowest-index keys equal to tau; thread-contiguous runs keep order
+        const int64_t run = (m + blockDim.x - 1) / blockDim.x;
+        const int64_t r0 = min(m, static_cast<int64_t>(tid) * run), r1 = min(m, r0 + run);
+        uint32_t tie_before = 0;
+        if (need != eq) {
+            uint32_t ties = 0;
+            for (int64_t i = r0; i < r1; ++i) {
+                uint32_t key;
+                int64_t index;
+                entry(i, key, index);
+                ties += key == tau ? 1u : 0u;
             }
-            __syncthreads();
-            const int per = (nwords + blockDim.x - 1) / blockDim.x;
-            const int wb = min(nwords, static_cast<int>(tid) * per), we = min(nwords, wb + per);
-            uint32_t c = 0;
-            for (int i = wb; i < we; ++i) c += __popc(S.bitmap[i]);
-            uint32_t pos = written + block_excl_scan(c, S.warp_tmp, &S.total);
-            for (int i = wb; i < we; ++i) {
-                uint32_t bits = S.bitmap[i];
-                while (bits) {
-                    const int b = __ffs(bits) - 1;
-                    bits &= bits - 1;
-                    if (pos < kk) out[pos] = static_cast<int32_t>(w0 + (static_cast<int64_t>(i) << 5) + b);
+            tie_before = block_excl_scan(ties, S.warp_tmp, &S.total);
+        }
+        const bool all_ties = need == eq;
+        uint32_t take_n = 0;
+        {
+            uint32_t tb = tie_before;
+            for (int64_t i = r0; i < r1; ++i) {
+                uint32_t key;
+                int64_t index;
+                entry(i, key, index);
+                const bool is_tie = key == tau;
+                take_n += key > tau || (is_tie && (all_ties || tb < need)) ? 1u : 0u;
+                tb += is_tie ? 1u : 0u;
+            }
+        }
+        uint32_t pos = block_excl_scan(take_n, S.warp_tmp, &S.total);
+        {
+            uint32_t tb = tie_before;
+            for (int64_t i = r0; i < r1; ++i) {
+                uint32_t key;
+                int64_t index;
+                entry(i, key, index);
+                const bool is_tie = key == tau;
+                if (key > tau || (is_tie && (all_ties || tb < need))) {
+                    if (pos < kk) out[pos] = static_cast<int32_t>(index);
                     ++pos;
                 }
+                tb += is_tie ? 1u : 0u;
             }
-            written += S.total;
-            __syncthreads();
         }
         for (int i = kk + tid; i < P.top_k; i += blockDim.x) out[i] = -1;
-        if (written != kk && tid == 0) raise_status(P.status, CSA_DEV_BAD_INDEX);
+        if (S.total != kk && tid == 0) raise_status(P.status, CSA_DEV_BAD_INDEX);
     }
     if (tid == 0) P.nsel_out[t] = static_cast<int32_t>(kk);
-    // ---- leave the workspace zeroed for the next call
-    if (!P.local_hist)
-        for (int i = tid; i < kD1Bins; i += blockDim.x) gh[i] = 0;
-    if (tid == 0) {
-        cnt->sel = 0;
-        cnt->cand = 0;
-        cnt->ticket = 0;
-    }
-    pdl_launch_dependents();
+    // ---- leave the per-token state zeroed for the next call (in one-CTA mode
+    // the histograms were built in shared memory, but the state is cleared all
+    // the same: it keeps the contract simple)
+    for (int i = tid; i < kD1Bins + kD2Bins; i += blockDim.x) gh[i] = 0;
+    if (tid == 0) cnt->ticket = 0;
+}
+
+void topk_grid(int64_t T, int64_t max_comp_rows, int32_t *chunk_out, int32_t *per_tok_out) {
+    const int64_t maxn = max_comp_rows > 0 ? max_comp_rows : 1;
+    // CTAs per token: about kTargetCtas in total, each with 1024 .. 4096 scores
+    const int64_t Tp = T > 0 ? T : 1;
+    const int64_t want = (kTargetCtas + Tp - 1) / Tp;
+    int64_t chunk = (maxn + want - 1) / want;
+    chunk = ((chunk + 1023) / 1024) * 1024;
+    if (chunk < 1024) chunk = 1024;
+    int64_t per_tok = (maxn + chunk - 1) / chunk;
+    if (chunk > kMaxFilterChunk || per_tok > kMaxPerTok) per_tok = 1;  // one CTA per token
+    if (per_tok == 1) chunk = maxn;
+    *chunk_out = static_cast<int32_t>(chunk);
+    *per_tok_out = static_cast<int32_t>(per_tok);
 }
 
 cudaError_t launch_topk(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
@@ -374,32 +461,29 @@ cudaError_t launch_topk(const Launch &lc, const csa_layout_t &L, const csa_param
     P.scores = scores;
     P.ld = ld;
     P.state = ws.state;
-    P.sel = ws.sel;
-    P.cand = ws.cand;
-    P.cap = ws.cap;
+    P.slots = ws.slots;
+    P.slot_cnt = ws.slot_cnt;
     P.idx_out = idx;
     P.nsel_out = n_sel;
     P.status = status;
-    const int64_t maxn = L.max_comp_rows > 0 ? L.max_comp_rows : 1;
-    // CTAs per token: enough to cover ~2 waves in total, each with >= 1024 scores.
-    int64_t want = (2 * static_cast<int64_t>(lc.sm_count) + T - 1) / T;
-    int64_t chunk = (maxn + want - 1) / want;
-    chunk = ((chunk + 1023) / 1024) * 1024;
-    if (chunk < 1024) chunk = 1024;
-    const int64_t per_tok = (maxn + chunk - 1) / chunk;
-    P.chunk = static_cast<int32_t>(chunk);
-    P.local_hist = (per_tok == 1 && !hist_ready) ? 1 : 0;
+    topk_grid(T, L.max_comp_rows, &P.chunk, &P.per_tok);
+    if (!P.slots || !P.slot_cnt) {  // no filter slots: one CTA owns each row
+        P.per_tok = 1;
+        P.chunk = static_cast<int32_t>(L.max_comp_rows > 0 ? L.max_comp_rows : 1);
+    }
+    P.local_hist = P.per_tok == 1 ? 1 : 0;
     cudaError_t e;
     if (!hist_ready && !P.local_hist) {
-        e = launch_pdl(score_hist_kernel, dim3(static_cast<unsigned>(per_tok), T), dim3(256), 0,
+        e = set_kernel_smem(score_hist_kernel, 0);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(score_hist_kernel, dim3(static_cast<unsigned>(P.per_tok), T), dim3(256), 0,
                        lc.stream, P);
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = sizeof(SelectSmem);
-    e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    const size_t smem = sizeof(SelectSmem) + 16;
+    e = set_kernel_smem(select_kernel, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(select_kernel, dim3(static_cast<unsigned>(per_tok), T), dim3(kSelThreads),
+    return launch_pdl(select_kernel, dim3(static_cast<unsigned>(P.per_tok), T), dim3(kSelThreads),
                       smem, lc.stream, P);
 }
 
