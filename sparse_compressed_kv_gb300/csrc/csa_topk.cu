@@ -177,6 +177,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
     if (!P.local_hist)
 #pragma unroll
         for (int u = 0; u < kD1Bins / kSelThreads; ++u) hreg[u] = __ldcg(&gh[u * kSelThreads + tid]);
+    // Multi-CTA mode: this CTA's slice [c0, c0 + chunk) is loaded now too, in
+    // coalesced warp spans (lane l of warp w holds index c0 + w*W + q*32 + l),
+    // bounded by the row capacity; entries past the visible count are masked
+    // once the layout is read.
+    const int span = ((P.chunk + kWarps - 1) / kWarps + 31) & ~31;  // W, at most 32 * kMaxPerThread
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * P.chunk;
+    const int64_t wbase = c0 + static_cast<int64_t>(warp) * span + lane;
+    uint32_t keys[kMaxPerThread];
+    if (!P.local_hist) {
+        const int64_t cend = min(c0 + P.chunk, P.L.max_comp_rows);
+        const float *row = P.scores + static_cast<int64_t>(t) * P.ld;
+#pragma unroll
+        for (int q = 0; q < kMaxPerThread; ++q) {
+            const int64_t i = wbase + q * 32;
+            keys[q] = (q * 32 < span && i < cend) ? score_key(__ldcg(row + i)) : 0u;
+        }
+    }
     const TokenView v = token_view(P.L, P.ratio, t);
     if (v.bad && blockIdx.x == 0 && tid == 0) raise_status(P.status, v.bad);
     const int64_t n = v.n_vis;
@@ -256,30 +273,38 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
                 }
             }
         } else {
-            // This CTA's slice: thread-contiguous runs kept in registers, so the
-            // block-wide scan writes the entries in ascending index order.
-            const int64_t b0 = static_cast<int64_t>(blockIdx.x) * P.chunk;
-            const int64_t b1 = min(n, b0 + P.chunk);
-            const int64_t my0 = b0 + static_cast<int64_t>(tid) * kMaxPerThread;
-            uint32_t keys[kMaxPerThread];
-            uint32_t mine = 0;
+            // This CTA's slice, already in registers: in index order (warp,
+            // q, lane), so a ballot per q and the warps' totals place every
+            // kept entry.
+            const int64_t b1 = min(n, c0 + P.chunk);
+            const unsigned lt = (1u << lane) - 1u;
+            uint32_t wt = 0;
 #pragma unroll
-            for (int e = 0; e < kMaxPerThread; ++e) {
-                const int64_t i = my0 + e;
-                keys[e] = i < b1 ? score_key(__ldcg(&sc[i])) : 0u;
-                const uint32_t dg = keys[e] >> kD1Shift;
-                mine += (i < b1 && dg >= d1) ? 1u : 0u;
-                if (i < b1 && dg == d1) atomicAdd(&gh2[(keys[e] >> kD2Shift) & (kD2Bins - 1)], 1u);
+            for (int q = 0; q < kMaxPerThread; ++q) {
+                const bool ok = q * 32 < span && wbase + q * 32 < b1;
+                const uint32_t dg = keys[q] >> kD1Shift;
+                wt += __popc(__ballot_sync(0xffffffffu, ok && dg >= d1));
+                if (ok && dg == d1) atomicAdd(&gh2[(keys[q] >> kD2Shift) & (kD2Bins - 1)], 1u);
             }
-            uint32_t pos = block_excl_scan(mine, S.warp_tmp, &S.total);
+            if (lane == 0) S.wcount[warp] = wt;
+            __syncthreads();
+            uint32_t pos = 0, total = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                const uint32_t x = S.wcount[w];
+                pos += w < warp ? x : 0u;
+                total += x;
+            }
             uint64_t *slot = P.slots + (static_cast<int64_t>(t) * P.per_tok + blockIdx.x) * P.chunk;
 #pragma unroll
-            for (int e = 0; e < kMaxPerThread; ++e) {
-                const int64_t i = my0 + e;
-                if (i < b1 && (keys[e] >> kD1Shift) >= d1)
-                    slot[pos++] = (static_cast<uint64_t>(keys[e]) << 32) | static_cast<uint32_t>(i);
+            for (int q = 0; q < kMaxPerThread; ++q) {
+                const bool keep = q * 32 < span && wbase + q * 32 < b1 && (keys[q] >> kD1Shift) >= d1;
+                const unsigned m = __ballot_sync(0xffffffffu, keep);
+                if (keep)
+                    slot[pos + __popc(m & lt)] = (static_cast<uint64_t>(keys[q]) << 32) |
+                                                 static_cast<uint32_t>(wbase + q * 32);
+                pos += __popc(m);
             }
-            if (tid == 0) P.slot_cnt[static_cast<int64_t>(t) * P.per_tok + blockIdx.x] = S.total;
+            if (tid == 0) P.slot_cnt[static_cast<int64_t>(t) * P.per_tok + blockIdx.x] = total;
         }
     }
 
@@ -319,29 +344,20 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
             }
             __syncthreads();
             if (!S.overflow) {
-                // addresses first (binary search over the slot prefix), then
-                // eight independent loads in flight per thread
+                // one thread per slot: its entries are contiguous, eight
+                // independent loads in flight at a time
                 const uint64_t *base = P.slots + static_cast<int64_t>(t) * pt * P.chunk;
-                const uint32_t ns = S.nstage;
-                for (uint32_t e0 = 0; e0 < ns; e0 += 8 * blockDim.x) {
-                    uint64_t val[8];
+                for (int sl = tid; sl < pt; sl += blockDim.x) {
+                    const uint32_t c = S.prefix[sl + 1] - S.prefix[sl];
+                    const uint64_t *src = base + static_cast<int64_t>(sl) * P.chunk;
+                    uint64_t *dst = S.stage + S.prefix[sl];
+                    for (uint32_t i0 = 0; i0 < c; i0 += 8) {
+                        uint64_t val[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t e = e0 + u * blockDim.x + tid;
-                        int lo = 0, hi = pt;  // prefix[lo] <= e < prefix[hi]
-                        while (hi - lo > 1) {
-                            const int mid = (lo + hi) >> 1;
-                            if (S.prefix[mid] <= e) lo = mid;
-                            else hi = mid;
-                        }
-                        val[u] = e < ns ? __ldcg(&base[static_cast<int64_t>(lo) * P.chunk +
-                                                      (e - S.prefix[lo])])
-                                        : 0ull;
-                    }
+                        for (int u = 0; u < 8; ++u) val[u] = i0 + u < c ? __ldcg(src + i0 + u) : 0ull;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t e = e0 + u * blockDim.x + tid;
-                        if (e < ns) S.stage[e] = val[u];
+                        for (int u = 0; u < 8; ++u)
+                            if (i0 + u < c) dst[i0 + u] = val[u];
                     }
                 }
             }
@@ -368,12 +384,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
         const uint32_t pre22 = (d1 << kD2Bits) | static_cast<uint32_t>(S.d);
         for (int i = tid; i < kD1Bins; i += blockDim.x) S.h[i] = 0;
         __syncthreads();
-        for (int64_t base = 0; base < m; base += blockDim.x) {
-            const int64_t i = base + tid;
-            uint32_t key = 0;
+        for (int64_t i = tid; i < m; i += blockDim.x) {
+            uint32_t key;
             int64_t index;
-            if (i < m) entry(i, key, index);
-            smem_hist_add(S.h, key & (kD3Bins - 1), i < m && (key >> kD2Shift) == pre22);
+            entry(i, key, index);
+            if ((key >> kD2Shift) == pre22) atomicAdd(&S.h[key & (kD3Bins - 1)], 1u);
         }
         __syncthreads();
         find_threshold_digit(S.h, kD1Bins, need, S.warp_tmp, &S.d, &S.gt);
