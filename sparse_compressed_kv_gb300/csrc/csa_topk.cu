@@ -51,32 +51,32 @@ struct SelectParams {
 
 // ---------------------------------------------------------------- helpers
 
-// Block-wide exclusive scan of one value per thread.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_tmp,
-                                                    uint32_t *total) {
+// Block-wide exclusive scan of one value per thread (32- or 64-bit).
+template <typename U>
+__device__ __forceinline__ U block_excl_scan(U v, U *warp_tmp, U *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t incl = v;
+    U incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        U y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
     if (lane == 31) warp_tmp[warp] = incl;
     __syncthreads();
     if (warp == 0) {
         const int nw = blockDim.x >> 5;
-        uint32_t x = lane < nw ? warp_tmp[lane] : 0u;
-        uint32_t xi = x;
+        U x = lane < nw ? warp_tmp[lane] : U(0);
+        U xi = x;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(0xffffffffu, xi, o);
+            U y = __shfl_up_sync(0xffffffffu, xi, o);
             if (lane >= o) xi += y;
         }
         if (lane < nw) warp_tmp[lane] = xi - x;
         if (lane == nw - 1 && total) *total = xi;
     }
     __syncthreads();
-    uint32_t r = warp_tmp[warp] + incl - v;
+    U r = warp_tmp[warp] + incl - v;
     __syncthreads();
     return r;
 }
@@ -91,7 +91,7 @@ __device__ void find_threshold_digit(const uint32_t *h, int nbins, uint32_t k, u
     const int hi = nbins - threadIdx.x * per;
     uint32_t local = 0;
     for (int b = hi - 1; b >= hi - per; --b) local += h[b];
-    uint32_t above = block_excl_scan(local, warp_tmp, nullptr);  // count in bins >= hi
+    uint32_t above = block_excl_scan<uint32_t>(local, warp_tmp, nullptr);  // count in bins >= hi
     uint32_t run = above;
     for (int b = hi - 1; b >= hi - per; --b) {
         const uint32_t c = h[b];
@@ -144,8 +144,11 @@ struct SelectSmem {
     uint32_t h[kD1Bins];           // digit-1 histogram, then digit-3 histogram
     uint32_t h2[kD2Bins];          // digit-2 histogram of the threshold bin
     uint32_t warp_tmp[32];
+    uint64_t warp_tmp64[32];
+    uint64_t total64;
     uint64_t stage[kStageCap];     // entries (key << 32 | index), ascending index
     uint32_t prefix[kMaxPerTok + 1];
+    uint32_t gprefix[kMaxPerTok + 1];  // staging groups of up to 8 entries per slot
     uint32_t wcount[32];           // one-CTA mode: entries per warp range
     uint32_t nstage;
     uint32_t overflow;
@@ -155,7 +158,8 @@ struct SelectSmem {
     uint32_t last;
 };
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams P) {
+// Two CTAs per SM: the filter grid (about two CTAs per SM) runs in one wave.
+__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectParams P) {
     extern __shared__ uint8_t smem_raw[];
     SelectSmem &S = *reinterpret_cast<SelectSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
@@ -335,30 +339,44 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
 #pragma unroll
             for (int u = 0; u < kD2Bins / kSelThreads; ++u)
                 S.h2[u * kSelThreads + tid] = __ldcg(&gh2[u * kSelThreads + tid]);
-            const uint32_t off = block_excl_scan(c, S.warp_tmp, &S.total);
-            if (tid < pt) S.prefix[tid] = off;
+            // entry offsets and staging-group offsets (groups of up to 8
+            // consecutive entries of one slot) in one packed scan
+            const uint64_t packed = (static_cast<uint64_t>((c + 7) / 8) << 32) | c;
+            const uint64_t off = block_excl_scan<uint64_t>(packed, S.warp_tmp64, &S.total64);
+            if (tid < pt) {
+                S.prefix[tid] = static_cast<uint32_t>(off);
+                S.gprefix[tid] = static_cast<uint32_t>(off >> 32);
+            }
             if (tid == 0) {
-                S.prefix[pt] = S.total;
-                S.nstage = S.total;
-                S.overflow = S.total > static_cast<uint32_t>(kStageCap);
+                const uint64_t tot = S.total64;
+                S.prefix[pt] = static_cast<uint32_t>(tot);
+                S.gprefix[pt] = static_cast<uint32_t>(tot >> 32);
+                S.nstage = static_cast<uint32_t>(tot);
+                S.overflow = (tot & 0xffffffffull) > static_cast<uint64_t>(kStageCap);
             }
             __syncthreads();
             if (!S.overflow) {
-                // one thread per slot: its entries are contiguous, eight
-                // independent loads in flight at a time
+                // one group per thread: its slot by one search over the group
+                // offsets, then up to eight independent loads in flight
                 const uint64_t *base = P.slots + static_cast<int64_t>(t) * pt * P.chunk;
-                for (int sl = tid; sl < pt; sl += blockDim.x) {
-                    const uint32_t c = S.prefix[sl + 1] - S.prefix[sl];
-                    const uint64_t *src = base + static_cast<int64_t>(sl) * P.chunk;
-                    uint64_t *dst = S.stage + S.prefix[sl];
-                    for (uint32_t i0 = 0; i0 < c; i0 += 8) {
-                        uint64_t val[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) val[u] = i0 + u < c ? __ldcg(src + i0 + u) : 0ull;
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            if (i0 + u < c) dst[i0 + u] = val[u];
+                const uint32_t ng = S.gprefix[pt];
+                for (uint32_t g = tid; g < ng; g += blockDim.x) {
+                    int lo = 0, hi = pt;  // the last slot with gprefix[lo] <= g
+                    while (hi - lo > 1) {
+                        const int mid = (lo + hi) >> 1;
+                        if (S.gprefix[mid] <= g) lo = mid;
+                        else hi = mid;
                     }
+                    const uint32_t e0 = (g - S.gprefix[lo]) * 8;
+                    const uint32_t cnt = S.prefix[lo + 1] - S.prefix[lo];
+                    const uint64_t *src = base + static_cast<int64_t>(lo) * P.chunk + e0;
+                    uint64_t *dst = S.stage + S.prefix[lo] + e0;
+                    uint64_t val[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) val[u] = e0 + u < cnt ? __ldcg(src + u) : 0ull;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (e0 + u < cnt) dst[u] = val[u];
                 }
             }
         }
@@ -408,7 +426,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
                 entry(i, key, index);
                 ties += key == tau ? 1u : 0u;
             }
-            tie_before = block_excl_scan(ties, S.warp_tmp, &S.total);
+            tie_before = block_excl_scan<uint32_t>(ties, S.warp_tmp, &S.total);
         }
         const bool all_ties = need == eq;
         uint32_t take_n = 0;
@@ -423,7 +441,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
                 tb += is_tie ? 1u : 0u;
             }
         }
-        uint32_t pos = block_excl_scan(take_n, S.warp_tmp, &S.total);
+        uint32_t pos = block_excl_scan<uint32_t>(take_n, S.warp_tmp, &S.total);
         {
             uint32_t tb = tie_before;
             for (int64_t i = r0; i < r1; ++i) {
