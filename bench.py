@@ -385,6 +385,40 @@ def run_ours(args, rank, world, device):
         if int(status.item()) != 0:
             raise RuntimeError("device status set in the HCA region")
 
+    # ---- prefill indexer alone: 4096 query tokens of one sequence share every
+    # key tile (four tokens per MMA), the tensor-bound case
+    prefill = None
+    if not args.no_prefill:
+        if "hd" in locals():
+            del hd, hgraphs, hgroup
+        torch.cuda.empty_cache()
+        pl = Layer(W.prefill(seed=900 + 1000 * rank, device=device), device, csa)
+        pw = pl.wl
+        psc = torch.empty(pw.num_tokens, pw.max_comp_rows, dtype=torch.float32, device=device)
+
+        def pstep():
+            csa.csa_indexer_scores(pl.layout, pl.prm, pl.d.q_idx, pl.d.w_idx, pl.d.k_idx, psc,
+                                   status, stream=stream)
+        with torch.cuda.stream(stream):
+            pstep()
+        torch.cuda.synchronize()
+        pgraph = capture(pstep, stream)
+        reps = max(3, min(20, args.steps // 10))
+        pms = time_graphs([pgraph], reps, 3, stream)
+        nvis = [min(int(pw.comp_off[1]), int(pw.tok_pos[t]) // pw.ratio)
+                for t in range(pw.num_tokens)]
+        flops = 2.0 * pw.n_ih * pw.ihd * float(sum(nvis))
+        tflops = flops / (pms * 1e-3) / 1e12
+        prefill = {"workload": "prefill: indexer alone, 4096 tokens at p = 262144.., "
+                               "65,536..66,559 visible blocks each, 64 heads x 128",
+                   "ms_per_launch": round(pms, 4), "tflops": round(tflops, 1),
+                   "peak_tflops": tf_peak, "peak_kind": peak_kind + " bf16 burst",
+                   "frac": round(tflops / tf_peak, 4), "launches": reps}
+        del psc, pl
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("device status set in the prefill region")
+
     tok_s = world * 1e3 / ms
     achieved = ab["indexer"] / (idx_ms * 1e-3) / 1e9
     line = {
@@ -414,6 +448,7 @@ def run_ours(args, rank, world, device):
         "clocks": clk,
         "batch32": batch,
         "hca": hca,
+        "prefill_indexer": prefill,
     }
     return line
 
@@ -525,6 +560,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-batch32", action="store_true")
     ap.add_argument("--no-hca", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
