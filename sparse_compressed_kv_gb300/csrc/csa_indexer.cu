@@ -33,7 +33,10 @@ struct IdxCfg {
     static constexpr int kBBytes = 2 * kBBox;             // queries of one unit
     static constexpr int kTmemCols = 2 * kN;              // two accumulators (power of two)
     static constexpr int kMaxUnits = 4096;
-    static constexpr int kThreads = 192;
+    // Epilogue warps: one per TMEM lane quarter; with several tokens per tile
+    // two per quarter, each taking half of the tokens.
+    static constexpr int kEpiWarps = G >= 2 ? 8 : 4;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kBarBytes = (2 * kStages + 6) * 8;
     static constexpr size_t kSmemMain = size_t(kStages) * kABytes + kBBytes;
     static size_t smem_bytes(bool hist) {
@@ -53,6 +56,7 @@ struct IndexerParams {
     int64_t ld;
     uint32_t *state;  // [T][kStateWords] when the digit-1 histogram is fused
     int32_t *status;
+    int32_t w_vec;    // w_idx 16-byte aligned: four weights per load
 };
 
 __device__ __forceinline__ int find_unit(const int32_t *prefix, int n, int u) {
@@ -66,7 +70,7 @@ __device__ __forceinline__ int find_unit(const int32_t *prefix, int n, int u) {
 }
 
 template <int G, bool kHist>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    const IndexerParams P) {
     using C = IdxCfg<G>;
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(b_empty, 1);
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 128);
+            mbar_init(&acc_empty[a], 32 * C::kEpiWarps);
         }
         mbar_fence_init();
         tma_prefetch_desc(&tm_k);
@@ -230,27 +234,30 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (128 threads)
+        // ------------------------------------------------ epilogue
         // No barrier inside this loop: a warp that gives up on a wait must not
         // strand the others.  Head weights are read through the read-only
-        // cache (one broadcast address per warp-load); the histogram keeps
-        // two per-unit slots in shared memory and sends later units straight
-        // to global memory.
+        // cache (one broadcast address per warp-load, four weights per load
+        // when aligned); the histogram keeps two per-unit slots in shared
+        // memory and sends later units straight to global memory.  With two
+        // warps per TMEM lane quarter, each takes half of the unit's tokens.
+        constexpr int kGPer = C::kEpiWarps == 8 ? G / 2 : G;
+        const int gbeg = C::kEpiWarps == 8 ? ((warp - 2) >> 2) * kGPer : 0;
         const int ep = threadIdx.x - 64;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const int first_unit = (u0 < u1) ? find_unit(prefix, nu, u0) : 0;
         int unit = first_unit, cur = -1, it = 0;
-        int64_t nv[G];
+        int64_t nv[kGPer];
 #pragma unroll
-        for (int g = 0; g < G; ++g) nv[g] = 0;
+        for (int g = 0; g < kGPer; ++g) nv[g] = 0;
         for (int u = u0; u < u1; ++u, ++it) {
             while (u >= prefix[unit + 1]) ++unit;
             if (unit != cur) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int t = unit * G + g;
+                for (int g = 0; g < kGPer; ++g) {
+                    const int t = unit * G + gbeg + g;
                     nv[g] = t < T ? token_view(P.L, P.ratio, t).n_vis : 0;
                 }
                 cur = unit;
@@ -262,7 +269,8 @@ __global__ void __launch_bounds__(192, 1)
             const int j = u - prefix[unit];
             const int64_t s = static_cast<int64_t>(j) * kTileKeys + row;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int gi = 0; gi < kGPer; ++gi) {
+                const int g = gbeg + gi;
                 const int t = unit * G + g;
                 if (t >= T) continue;  // warp-uniform
                 float v[4][16];
@@ -271,13 +279,28 @@ __global__ void __launch_bounds__(192, 1)
                 for (int c4 = 0; c4 < 4; ++c4) tmem_ld16(col + c4 * 16, v[c4]);
                 tmem_wait_ld();
                 const float *wt = P.w_idx + static_cast<int64_t>(t) * kNIH;
-                float score = 0.f;
+                float part[4] = {0.f, 0.f, 0.f, 0.f};  // four short chains, summed in order
+                if (P.w_vec) {
+                    const float4 *wt4 = reinterpret_cast<const float4 *>(wt);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
+                    for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        score = fmaf(__ldg(wt + c4 * 16 + i), fmaxf(v[c4][i], 0.f), score);
-                if (s < nv[g]) {
+                        for (int i = 0; i < 16; i += 4) {
+                            const float4 w4 = __ldg(wt4 + (c4 * 16 + i) / 4);
+                            part[c4] = fmaf(w4.x, fmaxf(v[c4][i + 0], 0.f), part[c4]);
+                            part[c4] = fmaf(w4.y, fmaxf(v[c4][i + 1], 0.f), part[c4]);
+                            part[c4] = fmaf(w4.z, fmaxf(v[c4][i + 2], 0.f), part[c4]);
+                            part[c4] = fmaf(w4.w, fmaxf(v[c4][i + 3], 0.f), part[c4]);
+                        }
+                } else {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            part[c4] = fmaf(__ldg(wt + c4 * 16 + i), fmaxf(v[c4][i], 0.f), part[c4]);
+                }
+                const float score = (part[0] + part[1]) + (part[2] + part[3]);
+                if (s < nv[gi]) {
                     P.scores[static_cast<int64_t>(t) * P.ld + s] = score;
                     if (kHist) {
                         const uint32_t bin = score_key(score) >> kD1Shift;
@@ -291,7 +314,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_arrive(&acc_empty[acc]);
         }
         if (kHist && u0 < u1) {
-            named_bar_sync(1, 128);
+            named_bar_sync(1, 32 * C::kEpiWarps);
             const int last_unit = find_unit(prefix, nu, u1 - 1);
             const int nslots = min(2, last_unit - first_unit + 1);
             for (int sl = 0; sl < nslots; ++sl) {
@@ -361,6 +384,7 @@ cudaError_t launch_indexer(const Launch &lc, const csa_layout_t &L, const csa_pa
     P.ld = ld;
     P.state = state;
     P.status = status;
+    P.w_vec = reinterpret_cast<uintptr_t>(w_idx) % 16 == 0 ? 1 : 0;  // rows are 256 B apart
     const int64_t tiles_bound =
         static_cast<int64_t>(P.num_units) * ((L.max_comp_rows + kTileKeys - 1) / kTileKeys);
     if (G == 4) return launch_g<4, false>(lc, tk, tq, P, tiles_bound);
