@@ -167,8 +167,11 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0 && u0 < u1) {
-            const uint64_t pol_k = policy_evict_first();
-            const uint64_t pol_q = policy_evict_last();
+            // One token per tile (decode): every key is read once, keep it
+            // out of the way.  Several tokens per tile (prefill): every unit
+            // of the sequence re-reads the same keys, keep them in L2.
+            const uint64_t pol_k = G > 1 ? policy_evict_last() : policy_evict_first();
+            const uint64_t pol_q = G > 1 ? policy_evict_normal() : policy_evict_last();
             int unit = find_unit(prefix, nu, u0), cur = -1;
             uint32_t gsw = 0;
             int64_t row_base = 0;
@@ -242,6 +245,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
         // memory and sends later units straight to global memory.  With two
         // warps per TMEM lane quarter, each takes half of the unit's tokens.
         constexpr int kGPer = C::kEpiWarps == 8 ? G / 2 : G;
+        const uint64_t pol_sc = G > 1 ? policy_evict_first() : 0ull;
         const int gbeg = C::kEpiWarps == 8 ? ((warp - 2) >> 2) * kGPer : 0;
         const int ep = threadIdx.x - 64;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
@@ -268,16 +272,25 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             tc_fence_after();
             const int j = u - prefix[unit];
             const int64_t s = static_cast<int64_t>(j) * kTileKeys + row;
+            // every TMEM load of the tile first, one wait, then the math
+            float v[kGPer][4][16];
+#pragma unroll
+            for (int gi = 0; gi < kGPer; ++gi) {
+                const uint32_t col = tmem_base + lane_addr +
+                                     static_cast<uint32_t>(acc * C::kN + (gbeg + gi) * 64);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) tmem_ld16(col + c4 * 16, v[gi][c4]);
+            }
+            tmem_wait_ld();
+            // the accumulator is in registers: hand it back to the MMA warp
+            // before the math
+            tc_fence_before();
+            mbar_arrive(&acc_empty[acc]);
 #pragma unroll
             for (int gi = 0; gi < kGPer; ++gi) {
                 const int g = gbeg + gi;
                 const int t = unit * G + g;
                 if (t >= T) continue;  // warp-uniform
-                float v[4][16];
-                const uint32_t col = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::kN + g * 64);
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld16(col + c4 * 16, v[c4]);
-                tmem_wait_ld();
                 const float *wt = P.w_idx + static_cast<int64_t>(t) * kNIH;
                 float part[4] = {0.f, 0.f, 0.f, 0.f};  // four short chains, summed in order
                 if (P.w_vec) {
@@ -287,21 +300,24 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 16; i += 4) {
                             const float4 w4 = __ldg(wt4 + (c4 * 16 + i) / 4);
-                            part[c4] = fmaf(w4.x, fmaxf(v[c4][i + 0], 0.f), part[c4]);
-                            part[c4] = fmaf(w4.y, fmaxf(v[c4][i + 1], 0.f), part[c4]);
-                            part[c4] = fmaf(w4.z, fmaxf(v[c4][i + 2], 0.f), part[c4]);
-                            part[c4] = fmaf(w4.w, fmaxf(v[c4][i + 3], 0.f), part[c4]);
+                            part[c4] = fmaf(w4.x, fmaxf(v[gi][c4][i + 0], 0.f), part[c4]);
+                            part[c4] = fmaf(w4.y, fmaxf(v[gi][c4][i + 1], 0.f), part[c4]);
+                            part[c4] = fmaf(w4.z, fmaxf(v[gi][c4][i + 2], 0.f), part[c4]);
+                            part[c4] = fmaf(w4.w, fmaxf(v[gi][c4][i + 3], 0.f), part[c4]);
                         }
                 } else {
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            part[c4] = fmaf(__ldg(wt + c4 * 16 + i), fmaxf(v[c4][i], 0.f), part[c4]);
+                            part[c4] = fmaf(__ldg(wt + c4 * 16 + i), fmaxf(v[gi][c4][i], 0.f), part[c4]);
                 }
                 const float score = (part[0] + part[1]) + (part[2] + part[3]);
                 if (s < nv[gi]) {
-                    P.scores[static_cast<int64_t>(t) * P.ld + s] = score;
+                    float *dst = P.scores + static_cast<int64_t>(t) * P.ld + s;
+                    // prefill rows (GBs) stream through L2 without displacing the keys
+                    if (G > 1) st_global_hint(dst, score, pol_sc);
+                    else *dst = score;
                     if (kHist) {
                         const uint32_t bin = score_key(score) >> kD1Shift;
                         const int slot = unit - first_unit;
@@ -310,8 +326,6 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&acc_empty[acc]);
         }
         if (kHist && u0 < u1) {
             named_bar_sync(1, 32 * C::kEpiWarps);
