@@ -31,6 +31,13 @@ constexpr int kSelThreads = 512;
 constexpr int kStageCap = 8192;        // entries staged in shared memory (64 KiB)
 static_assert(kStageCap % (kSelThreads / 32) == 0, "per-warp staging runs");
 constexpr int kMaxPerThread = kMaxFilterChunk / kSelThreads;
+// Resolver: the first kSpec entries of each of the first kSpecSlots slots (one
+// 128-byte line, the part a filter CTA has just written) are read together
+// with the slot counts, kSpecThreads threads per slot.
+constexpr int kSpecPer = 8;
+constexpr int kSpecThreads = 2;
+constexpr int kSpec = kSpecPer * kSpecThreads;
+constexpr int kSpecSlots = kSelThreads / kSpecThreads;
 
 struct SelectParams {
     csa_layout_t L;
@@ -332,16 +339,29 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
     } else {
         const uint32_t d1 = static_cast<uint32_t>(S.d);
         uint32_t need = kk - S.gt;   // >= 1, all from digit-1 bin d1
+        bool d2_found = false;
         if (!P.local_hist) {
-            // slot counts and the digit-2 histogram in one round trip
+            // One round trip: the slot counts, the digit-2 histogram and the
+            // first kSpec entries of every slot, read before their counts are
+            // known (entries past a slot's count are dropped below).
             const int pt = P.per_tok;
+            const uint64_t *base = P.slots + static_cast<int64_t>(t) * pt * P.chunk;
             const uint32_t c = tid < pt ? __ldcg(&P.slot_cnt[static_cast<int64_t>(t) * pt + tid]) : 0u;
+            uint32_t h2r[kD2Bins / kSelThreads];
 #pragma unroll
-            for (int u = 0; u < kD2Bins / kSelThreads; ++u)
-                S.h2[u * kSelThreads + tid] = __ldcg(&gh2[u * kSelThreads + tid]);
-            // entry offsets and staging-group offsets (groups of up to 8
-            // consecutive entries of one slot) in one packed scan
-            const uint64_t packed = (static_cast<uint64_t>((c + 7) / 8) << 32) | c;
+            for (int u = 0; u < kD2Bins / kSelThreads; ++u) h2r[u] = __ldcg(&gh2[u * kSelThreads + tid]);
+            const int ssl = tid / kSpecThreads;                     // slot of this thread's guess
+            const uint32_t se0 = (tid % kSpecThreads) * kSpecPer;  // its first entry
+            uint64_t sv[kSpecPer];
+#pragma unroll
+            for (int u = 0; u < kSpecPer; ++u)
+                sv[u] = ssl < pt ? __ldcg(base + static_cast<int64_t>(ssl) * P.chunk + se0 + u) : 0ull;
+#pragma unroll
+            for (int u = 0; u < kD2Bins / kSelThreads; ++u) S.h2[u * kSelThreads + tid] = h2r[u];
+            // entry offsets, and offsets of the groups of up to 8 entries the
+            // guesses did not cover, in one packed scan
+            const uint32_t spec = tid < pt && tid < kSpecSlots ? min(c, static_cast<uint32_t>(kSpec)) : 0u;
+            const uint64_t packed = (static_cast<uint64_t>((c - spec + 7) / 8) << 32) | c;
             const uint64_t off = block_excl_scan<uint64_t>(packed, S.warp_tmp64, &S.total64);
             if (tid < pt) {
                 S.prefix[tid] = static_cast<uint32_t>(off);
@@ -355,10 +375,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                 S.overflow = (tot & 0xffffffffull) > static_cast<uint64_t>(kStageCap);
             }
             __syncthreads();
+            // digit 2 needs only the histogram: find it now
+            find_threshold_digit(S.h2, kD2Bins, need, S.warp_tmp, &S.d, &S.gt);
+            d2_found = true;
             if (!S.overflow) {
-                // one group per thread: its slot by one search over the group
-                // offsets, then up to eight independent loads in flight
-                const uint64_t *base = P.slots + static_cast<int64_t>(t) * pt * P.chunk;
+                if (ssl < pt && ssl < kSpecSlots) {
+                    const uint32_t cnt = S.prefix[ssl + 1] - S.prefix[ssl];
+                    uint64_t *dst = S.stage + S.prefix[ssl];
+#pragma unroll
+                    for (int u = 0; u < kSpecPer; ++u)
+                        if (se0 + u < cnt) dst[se0 + u] = sv[u];
+                }
+                // the rest: one group per thread, its slot by one search over
+                // the group offsets, up to eight independent loads in flight
                 const uint32_t ng = S.gprefix[pt];
                 for (uint32_t g = tid; g < ng; g += blockDim.x) {
                     int lo = 0, hi = pt;  // the last slot with gprefix[lo] <= g
@@ -367,8 +396,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                         if (S.gprefix[mid] <= g) lo = mid;
                         else hi = mid;
                     }
-                    const uint32_t e0 = (g - S.gprefix[lo]) * 8;
                     const uint32_t cnt = S.prefix[lo + 1] - S.prefix[lo];
+                    const uint32_t sp = lo < kSpecSlots ? min(cnt, static_cast<uint32_t>(kSpec)) : 0u;
+                    const uint32_t e0 = sp + (g - S.gprefix[lo]) * 8;
                     const uint64_t *src = base + static_cast<int64_t>(lo) * P.chunk + e0;
                     uint64_t *dst = S.stage + S.prefix[lo] + e0;
                     uint64_t val[8];
@@ -397,7 +427,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
         };
         // ---- digit 2 from its histogram, then digit 3 over the few entries
         // that share digits 1 and 2
-        find_threshold_digit(S.h2, kD2Bins, need, S.warp_tmp, &S.d, &S.gt);
+        if (!d2_found) find_threshold_digit(S.h2, kD2Bins, need, S.warp_tmp, &S.d, &S.gt);
         need -= S.gt;
         const uint32_t pre22 = (d1 << kD2Bits) | static_cast<uint32_t>(S.d);
         for (int i = tid; i < kD1Bins; i += blockDim.x) S.h[i] = 0;
