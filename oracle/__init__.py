@@ -73,6 +73,12 @@ def _bind(lib):
     lib.csa_oracle_hca_decode.argtypes = [i32, i32, p, p, p, i32, i32, i32, i32, f64, p, p, i32,
                                           p, p, p, p, p]
     lib.csa_oracle_hca_decode.restype = i32
+    lib.csa_oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+    lib.csa_oracle_e2m1_value.restype = f64
+    lib.csa_oracle_fp4_quantize.argtypes = [i64, i32, p, p]
+    lib.csa_oracle_fp4_quantize.restype = i32
+    lib.csa_oracle_fp4_dequantize.argtypes = [i64, i32, p, p]
+    lib.csa_oracle_fp4_dequantize.restype = i32
     return lib
 
 
@@ -256,6 +262,35 @@ def _hca_decode(self, comp_kv, swa_kv, q, tok_seq, tok_pos, comp_off, swa_first_
 
 Oracle.hca_decode = _hca_decode
 
+FP4_ROW = 80  # bytes per MXFP4 key row (64 codes, 4 scales, 12 zero)
+
+
+def _e2m1_value(self, code: int) -> float:
+    return float(self._lib.csa_oracle_e2m1_value(int(code) & 0xFF))
+
+
+def _fp4_quantize(self, k_bits):
+    """bf16 key bits [R, 128] -> MXFP4 rows [R, 80] uint8."""
+    k_bits = _c(k_bits, np.uint16)
+    R, ihd = k_bits.shape
+    rows = np.zeros((R, FP4_ROW), dtype=np.uint8)
+    _check("fp4_quantize", self._lib.csa_oracle_fp4_quantize(R, ihd, _ptr(k_bits), _ptr(rows)))
+    return rows
+
+
+def _fp4_dequantize(self, rows, ihd: int = 128):
+    """MXFP4 rows [R, 80] -> bf16 key bits [R, 128] (exact)."""
+    rows = _c(rows, np.uint8)
+    R = rows.shape[0]
+    k = np.zeros((R, ihd), dtype=np.uint16)
+    _check("fp4_dequantize", self._lib.csa_oracle_fp4_dequantize(R, ihd, _ptr(rows), _ptr(k)))
+    return k
+
+
+Oracle.e2m1_value = _e2m1_value
+Oracle.fp4_quantize = _fp4_quantize
+Oracle.fp4_dequantize = _fp4_dequantize
+
 
 def default() -> Oracle:
     """The oracle built from csa_oracle.c (compiled on first use)."""
@@ -309,3 +344,15 @@ def decode(*args, **kwargs):
 
 def hca_decode(*args, **kwargs):
     return default().hca_decode(*args, **kwargs)
+
+
+def e2m1_value(*args, **kwargs):
+    return default().e2m1_value(*args, **kwargs)
+
+
+def fp4_quantize(*args, **kwargs):
+    return default().fp4_quantize(*args, **kwargs)
+
+
+def fp4_dequantize(*args, **kwargs):
+    return default().fp4_dequantize(*args, **kwargs)

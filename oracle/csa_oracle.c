@@ -350,3 +350,80 @@ done:
     free(kv_buf);
     return st;
 }
+
+/* ------------------------------------------------------------------ FP4 keys
+ * MXFP4 as read in csa_oracle.h: e2m1 elements, one e8m0 scale per 32. */
+static const double kE2m1Magnitude[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double csa_oracle_e2m1_value(uint8_t code) {
+    double v = kE2m1Magnitude[code & 7];
+    return (code & 8) ? -v : v;
+}
+
+/* Nearest e2m1 magnitude code to v >= 0 (v already divided by the block
+ * scale); of two equally near grid points the one with the even code wins;
+ * beyond the largest magnitude the code saturates. */
+static uint8_t e2m1_nearest(double v) {
+    if (v >= kE2m1Magnitude[7]) return 7;
+    uint8_t best = 0;
+    double best_d = fabs(v - kE2m1Magnitude[0]);
+    for (uint8_t c = 1; c < 8; ++c) {
+        double d = fabs(v - kE2m1Magnitude[c]);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+int32_t csa_oracle_fp4_quantize(int64_t R, int32_t ihd, const uint16_t *k, uint8_t *rows) {
+    if (R < 0 || ihd != 128 || (R > 0 && (!k || !rows))) return CSA_ORACLE_EINVAL;
+    for (int64_t r = 0; r < R; ++r) {
+        uint8_t *row = rows + r * CSA_ORACLE_FP4_ROW;
+        memset(row, 0, CSA_ORACLE_FP4_ROW);
+        for (int b = 0; b < ihd / 32; ++b) {
+            const uint16_t *x = k + r * ihd + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs(csa_oracle_bf16_to_f64(x[i]));
+                if (a > amax) amax = a;
+            }
+            int E = 0;
+            if (amax > 0.0) {
+                int ex;
+                frexp(amax, &ex);  /* amax = f * 2^ex, f in [0.5, 1): floor(log2) = ex - 1 */
+                E = (ex - 1) - 2 + 127;
+                if (E < 0) E = 0;
+                if (E > 254) E = 254;
+            }
+            row[64 + b] = (uint8_t)E;
+            const double scale = ldexp(1.0, E - 127);
+            for (int i = 0; i < 32; ++i) {
+                double v = csa_oracle_bf16_to_f64(x[i]);
+                uint8_t mag = e2m1_nearest(fabs(v) / scale);
+                uint8_t code = mag == 0 ? 0 : (uint8_t)(mag | (v < 0.0 ? 8 : 0));
+                int e = b * 32 + i;
+                row[e / 2] |= (uint8_t)((e & 1) ? (code << 4) : code);
+            }
+        }
+    }
+    return CSA_ORACLE_OK;
+}
+
+int32_t csa_oracle_fp4_dequantize(int64_t R, int32_t ihd, const uint8_t *rows, uint16_t *k) {
+    if (R < 0 || ihd != 128 || (R > 0 && (!k || !rows))) return CSA_ORACLE_EINVAL;
+    for (int64_t r = 0; r < R; ++r) {
+        const uint8_t *row = rows + r * CSA_ORACLE_FP4_ROW;
+        for (int e = 0; e < ihd; ++e) {
+            uint8_t code = (uint8_t)((e & 1) ? (row[e / 2] >> 4) : (row[e / 2] & 15));
+            double v = csa_oracle_e2m1_value(code) * ldexp(1.0, (int)row[64 + e / 32] - 127);
+            float f = (float)v;
+            uint32_t u;
+            memcpy(&u, &f, sizeof u);
+            if ((double)f != v || (u & 0xFFFFu) != 0) return CSA_ORACLE_EINVAL;
+            k[r * ihd + e] = (uint16_t)(u >> 16);
+        }
+    }
+    return CSA_ORACLE_OK;
+}

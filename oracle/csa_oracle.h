@@ -123,6 +123,31 @@ int32_t csa_oracle_hca_decode(int32_t T, int32_t num_seqs, const int32_t *tok_se
                               const int64_t *swa_first_pos, const uint16_t *q,
                               const float *sinks, int32_t *kv_len_out, double *out);
 
+/* FP4 indexer key cache.  [Audit rewrite], C4 and [Audit 1M], M1 cache the
+ * indexer keys in FP4 (the paper's section 5.2.1) without fixing a format.
+ * Reading: OCP MXFP4.  Elements are e2m1 (sign bit 3; exponent bits 2..1,
+ * bias 1; mantissa bit 0: 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives);
+ * every 32 consecutive elements share one e8m0 scale 2^(E - 127) with
+ * E = floor(log2(amax of the block)) - 2 + 127, clamped to 0 .. 254 (E = 0
+ * for an all-zero block).  An element is x / 2^(E-127) rounded to the
+ * nearest e2m1 magnitude, ties to the even code, saturating at 6; a zero
+ * magnitude is code 0 whatever the sign.
+ * One key row (ihd = 128): bytes 0..63 the codes (element 2i in the low
+ * nibble of byte i, element 2i+1 in the high nibble), bytes 64..67 the four
+ * block scales, bytes 68..79 zero: CSA_ORACLE_FP4_ROW bytes. */
+#define CSA_ORACLE_FP4_ROW 80
+
+/* Value of one e2m1 code (low 4 bits). */
+double csa_oracle_e2m1_value(uint8_t code);
+
+/* k [R, ihd] bf16 bits -> rows [R, CSA_ORACLE_FP4_ROW]; ihd must be 128. */
+int32_t csa_oracle_fp4_quantize(int64_t R, int32_t ihd, const uint16_t *k, uint8_t *rows);
+
+/* rows -> k [R, ihd] bf16 bits.  Every MXFP4 value of a quantized bf16 key is
+ * a bf16 value, so this is exact; a row whose values are not bf16 values
+ * (hand-made scales out of range) returns CSA_ORACLE_EINVAL. */
+int32_t csa_oracle_fp4_dequantize(int64_t R, int32_t ihd, const uint8_t *rows, uint16_t *k);
+
 #ifdef __cplusplus
 }
 #endif

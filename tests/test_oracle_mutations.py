@@ -59,6 +59,23 @@ MUTATIONS = [
      "o[d] += p * csa_oracle_bf16_to_f64(rows[((j + L - 1) % L) * hd + d]);"),
     ("HCA drops the newest visible block",
      "n_sel[t] = (int32_t)nv;", "n_sel[t] = (int32_t)(nv > 0 ? nv - 1 : 0);"),
+    ("FP4 ties go to the odd code",
+     "if (d < best_d || (d == best_d && (c & 1) == 0)) {",
+     "if (d < best_d || (d == best_d && (c & 1) == 1)) {"),
+    ("FP4 block scale one octave too high",
+     "E = (ex - 1) - 2 + 127;", "E = (ex - 1) - 1 + 127;"),
+    ("FP4 nibbles swapped",
+     "row[e / 2] |= (uint8_t)((e & 1) ? (code << 4) : code);",
+     "row[e / 2] |= (uint8_t)((e & 1) ? code : (code << 4));"),
+    ("FP4 sign dropped",
+     "uint8_t code = mag == 0 ? 0 : (uint8_t)(mag | (v < 0.0 ? 8 : 0));",
+     "uint8_t code = mag == 0 ? 0 : (uint8_t)(mag | 0);"),
+    ("FP4 block amax ignores negative elements",
+     "double a = fabs(csa_oracle_bf16_to_f64(x[i]));",
+     "double a = csa_oracle_bf16_to_f64(x[i]);"),
+    ("FP4 element rounded toward zero",
+     "if (v >= kE2m1Magnitude[7]) return 7;",
+     "if (v >= kE2m1Magnitude[7]) return 7;\n    for (uint8_t c = 7; c > 0; --c) if (kE2m1Magnitude[c] <= v) return c;"),
     ("sink added to the numerator side",
      "double zsink = sinks ? exp((double)sinks[h] - m) : 0.0;",
      "double zsink = sinks ? -0.5 * exp((double)sinks[h] - m) : 0.0;"),

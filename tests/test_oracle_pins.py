@@ -442,3 +442,153 @@ def test_memory_sizing_matches_pages():
     n1m = 262144
     assert n1m * W.IHD * 2 == g["indexer_key_bytes_1m"]
     assert n1m * W.HD * 2 == g["main_row_bytes_1m"]
+
+
+# ---------------------------------------------------------------- FP4 keys
+# MXFP4 as the oracle reads it (csa_oracle.h): e2m1 elements, one e8m0 scale
+# 2^(E-127) per 32 elements.  The pins below use the format's definition
+# (bit fields, the value grid) and properties any correct quantizer has.
+
+def e2m1_from_bits(c: int) -> float:
+    """OCP e2m1: sign bit 3, exponent bits 2..1 with bias 1, mantissa bit 0."""
+    s, e, m = (c >> 3) & 1, (c >> 1) & 3, c & 1
+    mag = m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1.0 + 0.5 * m)
+    return -mag if s else mag
+
+
+E2M1_GRID = np.array([e2m1_from_bits(c) for c in range(8)])
+
+
+def fp4_fields(rows: np.ndarray):
+    """codes [R, 128] (element 2i low nibble of byte i) and scales E [R, 4]."""
+    codes = np.empty((rows.shape[0], 128), dtype=np.uint8)
+    codes[:, 0::2] = rows[:, :64] & 15
+    codes[:, 1::2] = rows[:, :64] >> 4
+    return codes, rows[:, 64:68].astype(np.int64)
+
+
+def test_fp4_e2m1_table():
+    for c in range(16):
+        assert oracle.e2m1_value(c) == e2m1_from_bits(c), c
+    assert list(E2M1_GRID) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_fp4_grid_values_round_trip():
+    rng = np.random.default_rng(11)
+    R = 64
+    vals = np.zeros((R, 128))
+    for r in range(R):
+        for b in range(4):
+            s = int(rng.integers(-6, 6))
+            mags = rng.choice(E2M1_GRID, 32) * (2.0 ** s)
+            mags[int(rng.integers(0, 32))] = 6.0 * 2.0 ** s     # block amax 6 * 2^s: scale 2^s
+            signs = rng.choice([-1.0, 1.0], 32)
+            vals[r, b * 32:(b + 1) * 32] = signs * mags
+    bits = bf16_bits(vals)
+    assert np.array_equal(bits_to_f64(bits), vals)            # grid values are bf16 values
+    rows = oracle.fp4_quantize(bits)
+    assert rows.shape == (R, 80) and not rows[:, 68:].any()
+    # exact round trip (a signed zero comes back as +0: zero magnitude is code 0)
+    assert np.array_equal(bits_to_f64(oracle.fp4_dequantize(rows)), vals)
+    codes, E = fp4_fields(rows)
+    deq = np.array([[e2m1_from_bits(int(c)) for c in row] for row in codes])
+    assert np.array_equal(deq * 2.0 ** (np.repeat(E, 32, axis=1) - 127), vals)
+
+
+def test_fp4_nearest_code_ties_and_saturation():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((200, 128)) * np.exp(rng.uniform(-3, 3, (200, 1)))
+    bits = bf16_bits(x)
+    xv = bits_to_f64(bits)
+    rows = oracle.fp4_quantize(bits)
+    codes, E = fp4_fields(rows)
+    X = 2.0 ** (np.repeat(E, 32, axis=1) - 127)
+    chosen = np.vectorize(e2m1_from_bits)(codes)
+    # no e2m1 value (either sign) is nearer to x / X than the chosen one
+    cand = np.concatenate([E2M1_GRID, -E2M1_GRID])
+    best = np.abs(xv[..., None] / X[..., None] - cand).min(axis=-1)
+    assert (np.abs(xv / X - chosen) <= best).all()
+    # midpoints of the grid (block scale fixed at 2^0 by an element of 4):
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 7.75]
+    want = [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0, 6.0]      # even code, then saturation
+    blk = np.zeros(128)
+    blk[0] = 4.0
+    blk[1:1 + len(mids)] = mids
+    blk[32:32 + len(mids)] = -np.array(mids)
+    blk[64] = 7.75                                             # amax 7.75: scale still 2^0
+    r = oracle.fp4_quantize(bf16_bits(blk[None]))
+    c, e = fp4_fields(r)
+    assert e[0, 0] == 127 and e[0, 2] == 127
+    got = np.vectorize(e2m1_from_bits)(c[0])
+    assert list(got[1:1 + len(mids)]) == want
+    assert list(got[32:32 + len(mids)]) == [-w if w else 0.0 for w in want]
+    assert c[0, 32] == 0 and c[0, 64 + 1] == 0                 # a zero magnitude is code 0
+
+
+def test_fp4_scale_rule_and_zero_block():
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((100, 128)) * np.exp(rng.uniform(-20, 20, (100, 1)))
+    x[0, :32] = 0.0
+    x[1, 32:64] = -0.0
+    bits = bf16_bits(x)
+    rows = oracle.fp4_quantize(bits)
+    codes, E = fp4_fields(rows)
+    amax = np.abs(bits_to_f64(bits)).reshape(100, 4, 32).max(axis=-1)
+    X = 2.0 ** (E - 127)
+    nz = amax > 0
+    ratio = amax[nz] / X[nz]
+    assert ((ratio >= 4.0) & (ratio < 8.0)).all()
+    assert E[0, 0] == 0 and E[1, 1] == 0
+    assert not codes[0, :32].any() and not codes[1, 32:64].any()
+
+
+def test_fp4_sign_and_power_of_two_covariance():
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((50, 128))
+    bits = bf16_bits(x)
+    r0 = oracle.fp4_quantize(bits)
+    c0, e0 = fp4_fields(r0)
+    rn = oracle.fp4_quantize(bf16_bits(-bits_to_f64(bits)))
+    cn, en = fp4_fields(rn)
+    assert np.array_equal(en, e0)
+    assert np.array_equal(cn, np.where(c0 & 7, c0 ^ 8, 0))
+    r2 = oracle.fp4_quantize(bf16_bits(4.0 * bits_to_f64(bits)))
+    c2, e2 = fp4_fields(r2)
+    assert np.array_equal(c2, c0) and np.array_equal(e2, e0 + 2)
+
+
+def test_fp4_error_bound():
+    rng = np.random.default_rng(15)
+    bits = bf16_bits(rng.standard_normal((100, 128)))
+    x = bits_to_f64(bits)
+    rows = oracle.fp4_quantize(bits)
+    _, E = fp4_fields(rows)
+    X = 2.0 ** (np.repeat(E, 32, axis=1) - 127)
+    err = np.abs(x - bits_to_f64(oracle.fp4_dequantize(rows)))
+    inside = np.abs(x) <= 6.0 * X
+    assert (err[inside] <= 1.0 * X[inside]).all()     # half of the widest grid step (4 -> 6)
+    assert (err <= 2.0 * X).all()                      # saturation: |x| < 8 X
+    assert err.max() > 0
+
+
+def test_fp4_scores_are_the_indexer_on_dequantized_keys():
+    wl = W.tiny(seed=4)
+    qb, kb, w = W.bits(wl.q_idx), W.bits(wl.k_idx), wl.w_idx.numpy()
+    rows = oracle.fp4_quantize(kb)
+    kd = oracle.fp4_dequantize(rows)
+    sc, nv = oracle.indexer_scores(qb, w, kd, wl.tok_seq, wl.tok_pos, wl.comp_off)
+    q, k = bits_to_f64(qb), bits_to_f64(kd)
+    t = 0
+    n = int(nv[t])
+    ref = (np.maximum(np.einsum("hd,sd->hs", q[t], k[:n]), 0.0) * w[t].astype(np.float64)[:, None]).sum(0)
+    np.testing.assert_allclose(sc[t, :n], ref, rtol=1e-12, atol=1e-12)
+    # FP4 keys move the scores, but the ranking stays close to the bf16 one
+    sb, _ = oracle.indexer_scores(qb, w, kb, wl.tok_seq, wl.tok_pos, wl.comp_off)
+    assert np.corrcoef(sc[t, :n], sb[t, :n])[0, 1] > 0.9
+
+
+def test_fp4_row_size():
+    # 64 code bytes + 4 scale bytes + 12 zero bytes per 128-wide key; at 1M
+    # context (262,144 blocks) the indexer cache is 20 MiB instead of 64 MiB.
+    assert oracle.FP4_ROW == 80
+    assert 262144 * oracle.FP4_ROW == 20 * 2 ** 20
