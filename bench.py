@@ -39,8 +39,8 @@ UNIT = "tokens/s/layer"
 # committed ncu capture of that step (profiles/), and the SHA-256 prefix of the
 # kernel source it was taken on: once the source changes the figure no longer
 # describes the kernel, and the roofline reports traffic null.
-INDEXER_TRAFFIC_BYTES = 67161856 + 623616
-INDEXER_TRAFFIC_SOURCE = "5731632061f61fb2"
+INDEXER_TRAFFIC_BYTES = 67163392 + 583936
+INDEXER_TRAFFIC_SOURCE = "ebf76117f4a353d4"
 
 
 def indexer_traffic():
@@ -321,6 +321,51 @@ def run_ours(args, rank, world, device):
         e2e = {"value": round(world * 1e3 / e2e_ms, 1), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 4)}
 
+    # ---- next row: the same 1M step with the indexer keys cached as MXFP4
+    # (80 bytes per key instead of 256); the cache is quantized once, untimed
+    fp4 = None
+    if not args.no_fp4:
+        frows = []
+        for L in layers:
+            r = torch.empty(L.wl.k_idx.shape[0], csa.FP4_ROW, dtype=torch.uint8, device=device)
+            csa.csa_fp4_quantize_keys(L.d.k_idx, r, stream=stream)
+            frows.append(r)
+
+        def fstep(i, s):
+            L = layers[i]
+            csa.csa_decode_fp4(L.layout, L.prm, L.d.q_idx, L.d.w_idx, frows[i], L.d.comp_kv,
+                               L.d.q, L.out, status, ws, idx_out=L.idx, stream=s)
+
+        def findex_all():
+            for i, L in enumerate(layers):
+                csa.csa_indexer_scores_fp4(L.layout, L.prm, L.d.q_idx, L.d.w_idx, frows[i],
+                                           sc_buf, status, stream=stream)
+        with torch.cuda.stream(stream):
+            for i in range(len(layers)):
+                fstep(i, stream)
+            findex_all()
+        torch.cuda.synchronize()
+        fsingles = [capture(lambda i=i: fstep(i, stream), stream) for i in range(len(layers))]
+        fgroup = capture(lambda: [fstep(i, stream) for i in range(len(layers))], stream)
+        fms = time_steps(fgroup, fsingles, args.steps, args.warmup, stream)
+        figraph = capture(findex_all, stream)
+        fims = time_graphs([figraph], max(1, args.steps // len(layers)),
+                           max(1, args.warmup // len(layers)), stream) / len(layers)
+        nv = ab["keys"] // (wl0.ihd * 2)
+        fidx_bytes = nv * csa.FP4_ROW + (ab["indexer"] - ab["keys"])
+        fstep_bytes = ab["step"] - ab["keys"] + nv * csa.FP4_ROW
+        fp4 = {"workload": "1m with MXFP4 indexer keys (80 B per key: 20 MiB instead of 64 MiB)",
+               "tokens_per_s_per_layer": round(world * 1e3 / fms, 1),
+               "ms_per_step": round(fms, 5), "indexer_ms": round(fims, 5),
+               "indexer_bytes_per_launch": int(fidx_bytes),
+               "indexer_hbm_frac": round(fidx_bytes / (fims * 1e-3) / 1e9 / hbm_peak, 4),
+               "step_algorithmic_bytes": int(fstep_bytes),
+               "step_hbm_frac": round(fstep_bytes / (fms * 1e-3) / 1e9 / hbm_peak, 4)}
+        del fsingles, fgroup, figraph, frows
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("device status set in the FP4 region")
+
     # ---- secondary: batched decode, 32 ragged sequences (32K..128K)
     batch = None
     if not args.no_batch32:
@@ -449,6 +494,7 @@ def run_ours(args, rank, world, device):
         "batch32": batch,
         "hca": hca,
         "prefill_indexer": prefill,
+        "fp4": fp4,
     }
     return line
 
@@ -561,6 +607,7 @@ def main():
     ap.add_argument("--no-batch32", action="store_true")
     ap.add_argument("--no-hca", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-fp4", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -211,6 +211,41 @@ csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *para
                             const void *comp_kv, const void *q, const float *sinks, float *out,
                             int32_t *dev_status, void *ws, size_t ws_bytes, void *stream);
 
+/* FP4 indexer key cache ([Audit rewrite], C4, and [Audit 1M], M1: the
+ * indexer keys are cached in FP4, the paper's section 5.2.1).  The pages fix
+ * no format; this library reads it as OCP MXFP4: e2m1 elements (0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6 and negatives), one e8m0 scale 2^(E-127) per 32 elements
+ * with E = floor(log2(block amax)) - 2 + 127 (clamped to 0..254; 0 for an
+ * all-zero block), elements rounded to the nearest value, ties to the even
+ * code, saturating at 6, a zero stored as code 0.  One key (ihd = 128) is an
+ * 80-byte row: bytes 0..63 the codes (element 2i in the low nibble of byte
+ * i, 2i+1 in the high nibble), bytes 64..67 the four block scales, bytes
+ * 68..79 zero (rows stay 16-byte aligned for the bulk-copy engine).
+ *
+ * csa_fp4_quantize_keys: k_idx bf16 [rows, 128] -> k_fp4 uint8 [rows, 80],
+ * both device pointers, 16-byte aligned.  Row by row and deterministic, so a
+ * cache may quantize rows as it appends them.
+ *
+ * csa_indexer_scores_fp4 and csa_decode_fp4: csa_indexer_scores and
+ * csa_decode with the keys given as such rows (k_fp4 uint8 [R, 80]).  The
+ * scores are exactly those of the bf16 indexer on the dequantized keys
+ * (every MXFP4 value of a bf16 key is itself a bf16 value); the kernel reads
+ * 80 bytes per key instead of 256 and expands the codes in shared memory.
+ * Tokens are scored one per key tile (no grouping of prefill tokens).
+ * Same errors as the bf16 calls; k_fp4 must be 16-byte aligned. */
+csa_status_t csa_fp4_quantize_keys(int64_t rows, const void *k_idx, void *k_fp4, void *stream);
+
+csa_status_t csa_indexer_scores_fp4(const csa_layout_t *layout, const csa_params_t *params,
+                                    const void *q_idx, const float *w_idx, const void *k_fp4,
+                                    float *scores, int64_t ld_scores, int32_t *dev_status,
+                                    void *stream);
+
+csa_status_t csa_decode_fp4(const csa_layout_t *layout, const csa_params_t *params,
+                            const void *q_idx, const float *w_idx, const void *k_fp4,
+                            const void *comp_kv, const void *q, const float *sinks, float *out,
+                            int32_t *idx_out, int32_t *dev_status, void *ws, size_t ws_bytes,
+                            void *stream);
+
 /* csa_topk without a workspace, for callers that cannot allocate device
  * memory at all: an engine whose memory planner owns every byte of the GPU,
  * or a plug-in that is not allowed to call the allocator, cannot hand

@@ -27,7 +27,9 @@ DEV_CAPACITY, DEV_BAD_LENGTH, DEV_TIMEOUT = 0x08, 0x10, 0x20
 
 EXPORTS = ("csa_status_string", "csa_abi_version", "csa_workspace_size", "csa_indexer_scores",
            "csa_topk", "csa_gather_mixed", "csa_sparse_mqa_decode", "csa_decode",
-           "csa_hca_workspace_size", "csa_hca_decode")
+           "csa_hca_workspace_size", "csa_hca_decode", "csa_fp4_quantize_keys",
+           "csa_indexer_scores_fp4", "csa_decode_fp4")
+FP4_ROW = 80  # bytes per MXFP4 key row (include/csa.h)
 
 
 class CsaError(RuntimeError):
@@ -81,6 +83,9 @@ def load() -> ctypes.CDLL:
     lib.csa_decode.argtypes = [L, Pm, P, P, P, P, P, P, P, P, P, P, sz, P]
     lib.csa_hca_workspace_size.argtypes = [L, Pm, ctypes.POINTER(sz)]
     lib.csa_hca_decode.argtypes = [L, Pm, P, P, P, P, P, P, sz, P]
+    lib.csa_fp4_quantize_keys.argtypes = [i64, P, P, P]
+    lib.csa_indexer_scores_fp4.argtypes = [L, Pm, P, P, P, P, i64, P, P]
+    lib.csa_decode_fp4.argtypes = [L, Pm, P, P, P, P, P, P, P, P, P, P, sz, P]
     for fn in EXPORTS[2:]:
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
@@ -218,3 +223,26 @@ def csa_hca_decode(layout: Layout, prm: csa_params_t, comp_kv, q, out, dev_statu
     _check("csa_hca_decode", load().csa_hca_decode(
         ctypes.byref(lc), ctypes.byref(prm), _p(comp_kv), _p(q), _p(sinks), _p(out),
         _p(dev_status), _p(ws), int(ws.numel()), _stream(stream)))
+
+
+def csa_fp4_quantize_keys(k_idx, k_fp4, stream=None):
+    """bf16 keys [R, 128] -> MXFP4 rows [R, 80] uint8 (both on the GPU)."""
+    _check("csa_fp4_quantize_keys", load().csa_fp4_quantize_keys(
+        int(k_idx.shape[0]), _p(k_idx), _p(k_fp4), _stream(stream)))
+
+
+def csa_indexer_scores_fp4(layout: Layout, prm: csa_params_t, q_idx, w_idx, k_fp4, scores,
+                           dev_status, stream=None):
+    lc = layout.c()
+    _check("csa_indexer_scores_fp4", load().csa_indexer_scores_fp4(
+        ctypes.byref(lc), ctypes.byref(prm), _p(q_idx), _p(w_idx), _p(k_fp4), _p(scores),
+        int(scores.shape[1]), _p(dev_status), _stream(stream)))
+
+
+def csa_decode_fp4(layout: Layout, prm: csa_params_t, q_idx, w_idx, k_fp4, comp_kv, q, out,
+                   dev_status, ws, idx_out=None, sinks=None, stream=None):
+    lc = layout.c()
+    _check("csa_decode_fp4", load().csa_decode_fp4(
+        ctypes.byref(lc), ctypes.byref(prm), _p(q_idx), _p(w_idx), _p(k_fp4), _p(comp_kv), _p(q),
+        _p(sinks), _p(out), _p(idx_out), _p(dev_status), _p(ws), int(ws.numel()),
+        _stream(stream)))

@@ -64,9 +64,7 @@ static uint8_t *data_base(void *ws, size_t ws_bytes, const WsPlan &plan) {
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static std::once_flag g_encode_once;
 
-CUresult encode_tensor_map_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
-                                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                                   uint32_t box_outer) {
+static void resolve_encode() {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -75,6 +73,12 @@ CUresult encode_tensor_map_2d_bf16(CUtensorMap *map, const void *base, uint64_t 
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
+}
+
+CUresult encode_tensor_map_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
+                                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                                   uint32_t box_outer) {
+    resolve_encode();
     if (!g_encode) return CUDA_ERROR_NOT_SUPPORTED;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
@@ -84,6 +88,19 @@ CUresult encode_tensor_map_2d_bf16(CUtensorMap *map, const void *base, uint64_t 
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes,
+                                 uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+    resolve_encode();
+    if (!g_encode) return CUDA_ERROR_NOT_SUPPORTED;
+    cuuint64_t dims[2] = {inner_bytes, outer};
+    cuuint64_t strides[1] = {inner_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 // ---------------------------------------------------------------- device check
@@ -194,10 +211,10 @@ csa_status_t csa_workspace_size(const csa_layout_t *layout, const csa_params_t *
     return CSA_OK;
 }
 
-csa_status_t csa_indexer_scores(const csa_layout_t *layout, const csa_params_t *params,
-                                const void *q_idx, const float *w_idx, const void *k_idx,
-                                float *scores, int64_t ld_scores, int32_t *dev_status,
-                                void *stream) {
+static csa_status_t indexer_scores_impl(const csa_layout_t *layout, const csa_params_t *params,
+                                        const void *q_idx, const float *w_idx, const void *k_idx,
+                                        float *scores, int64_t ld_scores, int32_t *dev_status,
+                                        void *stream, bool fp4) {
     CSA_TRY(check_params(params));
     CSA_TRY(check_layout(layout, params, false));
     if (layout->num_tokens == 0) return CSA_OK;
@@ -209,7 +226,33 @@ csa_status_t csa_indexer_scores(const csa_layout_t *layout, const csa_params_t *
     CSA_TRY(current_device(&sms));
     Launch lc{static_cast<cudaStream_t>(stream), sms};
     return cuda_status(launch_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores,
-                                      ld_scores, nullptr, dev_status));
+                                      ld_scores, nullptr, dev_status, fp4));
+}
+
+csa_status_t csa_indexer_scores(const csa_layout_t *layout, const csa_params_t *params,
+                                const void *q_idx, const float *w_idx, const void *k_idx,
+                                float *scores, int64_t ld_scores, int32_t *dev_status,
+                                void *stream) {
+    return indexer_scores_impl(layout, params, q_idx, w_idx, k_idx, scores, ld_scores,
+                               dev_status, stream, false);
+}
+
+csa_status_t csa_indexer_scores_fp4(const csa_layout_t *layout, const csa_params_t *params,
+                                    const void *q_idx, const float *w_idx, const void *k_fp4,
+                                    float *scores, int64_t ld_scores, int32_t *dev_status,
+                                    void *stream) {
+    return indexer_scores_impl(layout, params, q_idx, w_idx, k_fp4, scores, ld_scores,
+                               dev_status, stream, true);
+}
+
+csa_status_t csa_fp4_quantize_keys(int64_t rows, const void *k_idx, void *k_fp4, void *stream) {
+    if (rows < 0) return CSA_ERR_INVALID_ARGUMENT;
+    if (rows == 0) return CSA_OK;
+    if (!k_idx || !k_fp4 || !aligned16(k_idx) || !aligned16(k_fp4)) return CSA_ERR_INVALID_ARGUMENT;
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    return cuda_status(launch_fp4_quantize(lc, rows, k_idx, k_fp4));
 }
 
 csa_status_t csa_topk(const csa_layout_t *layout, const csa_params_t *params, const float *scores,
@@ -283,10 +326,11 @@ csa_status_t csa_sparse_mqa_decode(int32_t num_tokens, const csa_params_t *param
                                         dev_status));
 }
 
-csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, const void *q_idx,
-                        const float *w_idx, const void *k_idx, const void *comp_kv, const void *q,
-                        const float *sinks, float *out, int32_t *idx_out, int32_t *dev_status,
-                        void *ws, size_t ws_bytes, void *stream) {
+static csa_status_t decode_impl(const csa_layout_t *layout, const csa_params_t *params,
+                                const void *q_idx, const float *w_idx, const void *k_idx,
+                                const void *comp_kv, const void *q, const float *sinks, float *out,
+                                int32_t *idx_out, int32_t *dev_status, void *ws, size_t ws_bytes,
+                                void *stream, bool fp4) {
     CSA_TRY(check_params(params));
     CSA_TRY(check_layout(layout, params, true));
     if (layout->num_tokens == 0) return CSA_OK;
@@ -307,7 +351,7 @@ csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, 
     int32_t *nsel = reinterpret_cast<int32_t *>(w + plan.off_nsel);
     const bool fuse = indexer_fuses_hist(*layout);
     cudaError_t e = launch_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores, plan.ld,
-                                   fuse ? state : nullptr, dev_status);
+                                   fuse ? state : nullptr, dev_status, fp4);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     TopkWs tw{state, reinterpret_cast<uint64_t *>(w + plan.off_slots),
               reinterpret_cast<uint32_t *>(w + plan.off_slot_cnt)};
@@ -327,6 +371,23 @@ csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, 
                                         reinterpret_cast<float *>(w + plan.off_part_o),
                                         reinterpret_cast<float *>(w + plan.off_part_ml),
                                         dev_status, true));
+}
+
+csa_status_t csa_decode(const csa_layout_t *layout, const csa_params_t *params, const void *q_idx,
+                        const float *w_idx, const void *k_idx, const void *comp_kv, const void *q,
+                        const float *sinks, float *out, int32_t *idx_out, int32_t *dev_status,
+                        void *ws, size_t ws_bytes, void *stream) {
+    return decode_impl(layout, params, q_idx, w_idx, k_idx, comp_kv, q, sinks, out, idx_out,
+                       dev_status, ws, ws_bytes, stream, false);
+}
+
+csa_status_t csa_decode_fp4(const csa_layout_t *layout, const csa_params_t *params,
+                            const void *q_idx, const float *w_idx, const void *k_fp4,
+                            const void *comp_kv, const void *q, const float *sinks, float *out,
+                            int32_t *idx_out, int32_t *dev_status, void *ws, size_t ws_bytes,
+                            void *stream) {
+    return decode_impl(layout, params, q_idx, w_idx, k_fp4, comp_kv, q, sinks, out, idx_out,
+                       dev_status, ws, ws_bytes, stream, true);
 }
 
 static int64_t hca_rows_max(const csa_layout_t *L, const csa_params_t *p) {

@@ -204,6 +204,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, int
         : "memory");
 }
 
+// Orders this thread's earlier generic-proxy writes of shared memory before
+// later async-proxy reads of it (TMA stores, tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_normal() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));

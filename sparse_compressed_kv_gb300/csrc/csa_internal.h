@@ -76,9 +76,14 @@ struct RowSource {
     const void *comp_kv;           // fused: bf16 [R][hd]
 };
 
+// k_idx: bf16 [R, 128] keys, or, with fp4, MXFP4 rows [R, 80] (csa.h).
 cudaError_t launch_indexer(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
                            const void *q_idx, const float *w_idx, const void *k_idx,
-                           float *scores, int64_t ld, uint32_t *state, int32_t *status);
+                           float *scores, int64_t ld, uint32_t *state, int32_t *status,
+                           bool fp4 = false);
+
+// bf16 keys [R, 128] -> MXFP4 rows [R, 80].
+cudaError_t launch_fp4_quantize(const Launch &lc, int64_t rows, const void *k_idx, void *k_fp4);
 
 // True when csa_decode's indexer can fold the pass-1 histogram of the top-k
 // into its epilogue (one token per indexer unit).
@@ -132,5 +137,8 @@ cudaError_t set_kernel_smem(K kernel, size_t dyn_bytes) {
 CUresult encode_tensor_map_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
                                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                                    uint32_t box_outer);
+// Dense byte rows of inner_bytes each, no swizzle.
+CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes,
+                                 uint64_t outer, uint32_t box_inner, uint32_t box_outer);
 
 }  // namespace csa
