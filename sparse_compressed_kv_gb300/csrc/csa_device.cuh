@@ -195,6 +195,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
 
 // 2-D tiled load of one box into shared memory, completing on `bar`.
 // x (innermost coordinate, elements) must keep x * elem_size a multiple of 16.
+// Warm L2 with one box of a tensor: nothing lands in shared memory and
+// nothing waits for it.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, int32_t x, int32_t y,
                                             uint64_t *bar, uint64_t policy) {
     asm volatile(

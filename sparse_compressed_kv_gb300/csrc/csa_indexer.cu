@@ -182,6 +182,23 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp4>::kThreads, 1)
 
     // Inputs may come from the preceding grid in the stream.
     pdl_wait();
+    // One sequence, one unit: while the layout is read, warm L2 with this
+    // CTA's first key tiles as they fall when the sequence starts at row 0 and
+    // fills the cache.  A guess: a layout that says otherwise costs bandwidth,
+    // never data (nothing is read from this warming).
+    if (threadIdx.x == 0 && nu == 1 && P.L.num_seqs == 1) {
+        const int Us = static_cast<int>((P.L.max_comp_rows + kTileKeys - 1) / kTileKeys);
+        const int s0 = static_cast<int>(static_cast<int64_t>(Us) * blockIdx.x / gridDim.x);
+        const int s1 = static_cast<int>(static_cast<int64_t>(Us) * (blockIdx.x + 1) / gridDim.x);
+        for (int u = s0; u < s1 && u < s0 + 4; ++u) {
+            if constexpr (kFp4) {
+                tma_prefetch_l2_2d(&tm_k, 0, u * kTileKeys);
+            } else {
+                tma_prefetch_l2_2d(&tm_k, 0, u * kTileKeys);
+                tma_prefetch_l2_2d(&tm_k, 64, u * kTileKeys);
+            }
+        }
+    }
 
     // Tiles per unit -> exclusive prefix over units.
     if (threadIdx.x == 0) prefix[0] = 0;
