@@ -34,6 +34,13 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     const int64_t per = (chunks + splits - 1) / splits;
     w.rows_split = static_cast<int32_t>(per * kAttnChunk);
     w.splits = static_cast<int32_t>((rows_max + w.rows_split - 1) / w.rows_split);
+    // When a token's splits fit one portable cluster (at most 8 CTAs), they
+    // merge their partials through distributed shared memory and write the
+    // output: no partials in global memory and no combine kernel.  With more
+    // splits the partials go through L2 to the combine: on-chip exchange of
+    // that volume is no faster than L2, and a merge per cluster would only
+    // add a step.
+    w.attn_cluster = (w.splits >= 2 && w.splits <= 8) ? w.splits : 1;
     const size_t A = 256;
     const size_t Tz = static_cast<size_t>(T > 0 ? T : 0);
     w.state_bytes = Tz * kStateWords * 4;

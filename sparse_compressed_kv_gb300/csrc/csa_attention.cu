@@ -13,8 +13,10 @@
 // M5), QK^T and PV run on mma.sync bf16 tensor-core tiles with f32
 // accumulation, and the softmax is online across chunks with warp-shuffle
 // reductions.  Each row is read once for all 16 heads of the CTA.  With more
-// than one split per token, a combine kernel merges the partial (m, l, O)
-// with log-sum-exp weights.
+// than one split per token, the splits run in thread-block clusters of up to 8
+// neighbouring CTAs that merge their partial (m, l, O) through distributed
+// shared memory with log-sum-exp weights; when more than one cluster covers a
+// token, a combine kernel merges the clusters' partials the same way.
 #include <math.h>
 
 #include "csa_device.cuh"
@@ -22,10 +24,12 @@
 
 namespace csa {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;  // 8 warps
 constexpr int kRowBytes = kHD * 2;  // 1 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 64;   // attention splits per token (the plan never exceeds it)
+constexpr int kCombineParts = 4;  // combine CTAs per (token, head): 128 columns each
+constexpr int kMaxCluster = 8;    // attention CTAs per cluster (portable limit)
 
 // Row count of token t and the address of its row j (nullptr: skipped row).
 struct TokRows {
@@ -55,6 +59,8 @@ __device__ __forceinline__ TokRows token_rows(const RowSource &R, int t) {
         r.len = len;
         return r;
     }
+    // the selection count does not depend on the layout: load it alongside
+    const int32_t ns_sel = R.fused == kRowsSelected ? R.n_sel[t] : 0;
     TokenView v = token_view(R.L, R.ratio, t);
     r.bad = v.bad;
     if (v.bad & CSA_DEV_BAD_LAYOUT) {
@@ -65,7 +71,7 @@ __device__ __forceinline__ TokRows token_rows(const RowSource &R, int t) {
     if (R.fused == kRowsAllVisible) {
         ns = static_cast<int32_t>(v.n_vis);   // every visible block, in index order
     } else {
-        ns = R.n_sel[t];
+        ns = ns_sel;
         if (ns < 0 || ns > R.top_k) {
             r.bad |= CSA_DEV_BAD_LENGTH;
             ns = ns < 0 ? 0 : R.top_k;
@@ -80,14 +86,22 @@ __device__ __forceinline__ TokRows token_rows(const RowSource &R, int t) {
     return r;
 }
 
-__device__ __forceinline__ const __nv_bfloat16 *row_ptr(const RowSource &R, const TokRows &tr,
-                                                         int t, int j, int *bad) {
+// Compressed-cache index of selected row j (j < top_k; padding entries past
+// the token's selection count hold -1 and are never used).  It needs no
+// token record, so a caller may load it before the record arrives.
+__device__ __forceinline__ int32_t sel_index(const RowSource &R, int t, int j) {
+    if (R.fused == kRowsAllVisible) return j;
+    if (R.fused == kRowsSelected && j < R.top_k) return R.idx[static_cast<int64_t>(t) * R.top_k + j];
+    return 0;
+}
+
+// Address of row j given its preloaded selection index s (used when j < n_sel).
+__device__ __forceinline__ const __nv_bfloat16 *row_ptr_at(const RowSource &R, const TokRows &tr,
+                                                            int t, int j, int32_t s, int *bad) {
     if (R.fused == kRowsGathered)
         return static_cast<const __nv_bfloat16 *>(R.kv_buf) +
                (static_cast<int64_t>(t) * R.rows_per_token + j) * kHD;
     if (j < tr.n_sel) {
-        const int32_t s =
-            R.fused == kRowsAllVisible ? j : R.idx[static_cast<int64_t>(t) * R.top_k + j];
         if (s < 0 || s >= tr.n_vis) {
             *bad |= CSA_DEV_BAD_INDEX;
             return nullptr;
@@ -102,6 +116,12 @@ __device__ __forceinline__ const __nv_bfloat16 *row_ptr(const RowSource &R, cons
     const int64_t slot = x % R.L.swa_cap;
     return static_cast<const __nv_bfloat16 *>(R.L.swa_kv) +
            (static_cast<int64_t>(tr.b) * R.L.swa_cap + slot) * kHD;
+}
+
+__device__ __forceinline__ const __nv_bfloat16 *row_ptr(const RowSource &R, const TokRows &tr,
+                                                         int t, int j, int *bad) {
+    const int32_t s = (R.fused != kRowsGathered && j < tr.n_sel) ? sel_index(R, t, j) : 0;
+    return row_ptr_at(R, tr, t, j, s, bad);
 }
 
 // ---------------------------------------------------------------- gather
@@ -143,6 +163,7 @@ struct AttnParams {
     int32_t H;
     int32_t splits;
     int32_t rows_split;
+    int32_t cluster;         // CTAs per cluster along the splits (divides splits)
     float scale_log2;        // scale * log2(e)
     const __nv_bfloat16 *q;  // [T][H][512]
     const float *sinks;      // [H] or null
@@ -157,13 +178,17 @@ struct AttnParams {
 
 struct AttnSmem {
     __nv_bfloat16 q[kHeadGroup * kHD];              // 16 KiB, 16-byte chunks xor-swizzled by row
-    __nv_bfloat16 rows[2][kAttnChunk * kHD];        // 2 x 32 KiB, same swizzle
+    __nv_bfloat16 rows[2][kAttnChunk * kHD];        // 2 x 32 KiB, same swizzle; rows[0]
+                                                    // stages the f32 output at the end
     const __nv_bfloat16 *ptr[2][kAttnChunk];
-    float s[kHeadGroup][kAttnChunk];                // logits of the chunk (log2 units)
+    float s[2][kHeadGroup][kAttnChunk];             // QK^T of the chunk, one per half of hd
     // probabilities as two bf16 terms, p = hi + lo (padded rows): the PV product
     // keeps ~16 bits of each weight instead of bf16's 8
     __nv_bfloat16 p[2][kHeadGroup][kAttnChunk + 8];
     float m[kHeadGroup], l[kHeadGroup], alpha[kHeadGroup];
+    float wc[8][kHeadGroup];    // cluster merge: weight of each rank's partial per head
+    float fin[kHeadGroup];      // cluster merge: output scale per head
+    float mc[kHeadGroup], lc[kHeadGroup];
     TokRows tr;
 };
 
@@ -198,6 +223,108 @@ __device__ __forceinline__ void issue_chunk(AttnSmem &S, const RowSource &R, int
     issue_chunk_copies(S, R, buf);
 }
 
+// Merge of the cluster's partials (every CTA has staged its unnormalised O in
+// rows[0], f32 [16][512] with 16-byte chunks xor-swizzled by head, and its m,
+// l per head).  Rank r combines chunk range r/C of the 16 x 128 chunks from
+// every rank's staging area; the result is the cluster's partial in slot
+// split / C, or, when one cluster covers all of the token's splits (the
+// plan's choice), the normalised output (with the sink in the denominator).
+__device__ __forceinline__ void cluster_merge(const AttnParams &A, AttnSmem &S, int t, int split,
+                                           int h0, int bad) {
+    const int C = A.cluster;
+    const uint32_t rank = cluster_ctarank();
+    const bool final = C == A.splits;
+    cluster_sync_all();   // every rank's staging, m and l are written
+    if (threadIdx.x < kHeadGroup) {
+        const int h = threadIdx.x;
+        // every remote load is issued before any is used: the loads are
+        // ordered, so a use between them would serialise the round trips
+        float mr[kMaxCluster], lr[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+            mr[r] = -INFINITY;
+            lr[r] = 0.f;
+            if (r < C) {
+                mr[r] = ld_cluster_f32(cluster_map(&S.m[h], r));
+                lr[r] = ld_cluster_f32(cluster_map(&S.l[h], r));
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, mr[r]);
+        float L = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+            const float w = mr[r] == -INFINITY ? 0.f : exp2f(mr[r] - M);
+            if (r < C) S.wc[r][h] = w;
+            L += w * lr[r];
+        }
+        S.mc[h] = M;
+        S.lc[h] = L;
+        if (final) {
+            // out = O / (L + 2^(sink - M)), scaled against max(M, sink)
+            const float sk = A.sinks ? A.sinks[h0 + h] * kLog2e : -INFINITY;
+            const float Mall = fmaxf(M, sk);
+            const float sM = M == -INFINITY ? 0.f : exp2f(M - Mall);
+            const float z = L * sM + (A.sinks ? exp2f(sk - Mall) : 0.f);
+            S.fin[h] = z > 0.f ? sM / z : 0.f;
+        } else {
+            S.fin[h] = 1.f;
+        }
+    }
+    __syncthreads();
+    const float *stg = reinterpret_cast<const float *>(S.rows[0]);
+    constexpr int kChunks = kHeadGroup * (kHD / 4);
+    const int e0 = static_cast<int>((static_cast<int64_t>(kChunks) * rank) / C);
+    const int e1 = static_cast<int>((static_cast<int64_t>(kChunks) * (rank + 1)) / C);
+    const int64_t slot = split / C;
+    const int64_t pbase = (static_cast<int64_t>(t) * A.splits + slot) * A.H + h0;
+    float *dst = final ? A.out + (static_cast<int64_t>(t) * A.H + h0) * kHD : A.part_o + pbase * kHD;
+    const bool vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+    for (int e = e0 + threadIdx.x; e < e1; e += kAttnThreads) {
+        const int h = e / (kHD / 4), ch = e % (kHD / 4);
+        const float *src = stg + h * kHD + ((ch ^ (h & 7)) << 2);
+        float4 v[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+            if (r < C) v[r] = ld_cluster_v4f32(cluster_map(src, r));
+        // a rank without rows (weight 0) staged nothing: its values are skipped
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+            if (r < C) {
+                const float w = S.wc[r][h];
+                if (w != 0.f) {
+                    acc.x += w * v[r].x;
+                    acc.y += w * v[r].y;
+                    acc.z += w * v[r].z;
+                    acc.w += w * v[r].w;
+                }
+            }
+        }
+        const float f = S.fin[h];
+        acc.x *= f;
+        acc.y *= f;
+        acc.z *= f;
+        acc.w *= f;
+        float *d = dst + h * kHD + ch * 4;
+        if (vec) {
+            *reinterpret_cast<float4 *>(d) = acc;
+        } else {
+            d[0] = acc.x;
+            d[1] = acc.y;
+            d[2] = acc.z;
+            d[3] = acc.w;
+        }
+    }
+    if (!final && rank == 0 && threadIdx.x < kHeadGroup) {
+        A.part_ml[(pbase + threadIdx.x) * 2 + 0] = S.mc[threadIdx.x];
+        A.part_ml[(pbase + threadIdx.x) * 2 + 1] = S.lc[threadIdx.x];
+    }
+    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+    raise_status(A.status, bad);
+}
+
 __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParams A) {
     extern __shared__ uint8_t smem_raw[];
     AttnSmem &S = *reinterpret_cast<AttnSmem *>(
@@ -220,30 +347,44 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
     pdl_wait();
     pdl_launch_dependents();
 
-    // Warp 0 resolves the token's rows and the first chunk's row addresses in
-    // one pass (every lane reads the same token record: a broadcast).
+    // Warp 0 resolves the token's rows and the first chunk's row addresses.
+    // The chunk's selection indices, the selection count and the layout
+    // record are independent loads, issued together; only the sequence's
+    // offsets wait for the record.
     const int r_begin = split * A.rows_split;
     int bad = 0;
     if (warp == 0) {
+        const int j = r_begin + lane;
+        const int32_t s_pre = sel_index(A.R, t, j);
         const TokRows tr = token_rows(A.R, t);
         if (lane == 0) S.tr = tr;
         const int re = min(tr.len, r_begin + A.rows_split);
-        const int j = r_begin + lane;
-        S.ptr[0][lane] = j < re ? row_ptr(A.R, tr, t, j, &bad) : nullptr;
+        S.ptr[0][lane] = j < re ? row_ptr_at(A.R, tr, t, j, s_pre, &bad) : nullptr;
         if (lane == 0 && split == 0 && hg == 0) bad |= tr.bad;
     }
     __syncthreads();
     const int len = S.tr.len;
     const int r_end = min(len, r_begin + A.rows_split);
 
-    if (r_begin >= r_end) {
+    const bool empty = r_begin >= r_end;
+    if (empty) {
         if (A.early_q) cp_async_wait<0>();
-        // nothing here; with one split this CTA still owns the output (zeros)
-        if (A.splits == 1) {
-            float *o = A.out + (static_cast<int64_t>(t) * A.H + h0) * kHD;
-            for (int i = threadIdx.x; i < kHeadGroup * kHD; i += kAttnThreads) o[i] = 0.f;
+        if (A.cluster == 1) {
+            // nothing here; with one split this CTA still owns the output (zeros)
+            if (A.splits == 1) {
+                float *o = A.out + (static_cast<int64_t>(t) * A.H + h0) * kHD;
+                for (int i = threadIdx.x; i < kHeadGroup * kHD; i += kAttnThreads) o[i] = 0.f;
+            }
+            raise_status(A.status, bad);
+            return;
         }
-        raise_status(A.status, bad);
+        // in a cluster the CTA still takes part in the merge, with no rows
+        if (threadIdx.x < kHeadGroup) {
+            S.m[threadIdx.x] = -INFINITY;
+            S.l[threadIdx.x] = 0.f;
+        }
+        __syncthreads();
+        cluster_merge(A, S, t, split, h0, bad);
         return;
     }
     if (!A.early_q) load_q();
@@ -254,9 +395,10 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
     const int nchunks = (r_end - r_begin + kAttnChunk - 1) / kAttnChunk;
     issue_chunk_copies(S, A.R, 0);
 
-    float o[16][4];
+    // Output columns 64w .. 64w+63 of all 16 heads: 8 n8 tiles.
+    float o[8][4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
     const uint32_t q_base = smem_addr(S.q);
     const uint32_t p_base = smem_addr(&S.p[0][0][0]);
@@ -274,67 +416,67 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
         __syncthreads();
         const uint32_t rows_base = smem_addr(S.rows[buf]);
 
-        // ---- logits: warp w owns rows 8w..8w+7 of the chunk, all 16 heads
+        // ---- QK^T: warp w owns rows 8(w%4) .. +7 of the chunk, all 16 heads,
+        // and half w/4 of the 512 dimensions; the halves add in the softmax
         {
-            // two independent accumulation chains (even / odd k-steps)
             float sacc[4] = {0.f, 0.f, 0.f, 0.f};
             float sacc2[4] = {0.f, 0.f, 0.f, 0.f};
-            const int rr = warp * 8 + (lane & 7);
+            const int rr = (warp & 3) * 8 + (lane & 7);
             const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int kb = (warp >> 2) * (kHD / 32);
 #pragma unroll 4
-            for (int kk = 0; kk < kHD / 16; kk += 2) {
+            for (int kk = 0; kk < kHD / 32; kk += 2) {
+                const int k = kb + kk;
                 uint32_t a0, a1, a2, a3, e0, e1, e2, e3, b0, b1, b2, b3;
-                ldsm_x4(q_base + swz(qr, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
-                ldsm_x4(q_base + swz(qr, (kk + 1) * 2 + (lane >> 4)), e0, e1, e2, e3);
-                ldsm_x4(rows_base + swz(rr, kk * 2 + (lane >> 3)), b0, b1, b2, b3);
+                ldsm_x4(q_base + swz(qr, k * 2 + (lane >> 4)), a0, a1, a2, a3);
+                ldsm_x4(q_base + swz(qr, (k + 1) * 2 + (lane >> 4)), e0, e1, e2, e3);
+                ldsm_x4(rows_base + swz(rr, k * 2 + (lane >> 3)), b0, b1, b2, b3);
                 mma_bf16_16816(sacc, a0, a1, a2, a3, b0, b1);
                 mma_bf16_16816(sacc2, e0, e1, e2, e3, b2, b3);
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];
             // c-fragment: heads g, g+8; rows 2c, 2c+1 of this warp's 8
+            float(&sp)[kHeadGroup][kAttnChunk] = S.s[warp >> 2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int head = g + (e >> 1) * 8;
-                const int col = warp * 8 + 2 * c + (e & 1);
-                const bool valid = r0 + col < r_end && S.ptr[buf][col] != nullptr;
-                S.s[head][col] = valid ? sacc[e] * A.scale_log2 : -INFINITY;
+            for (int e = 0; e < 4; ++e)
+                sp[g + (e >> 1) * 8][(warp & 3) * 8 + 2 * c + (e & 1)] = sacc[e] + sacc2[e];
+        }
+        __syncthreads();
+
+        // ---- online softmax: warp w owns heads 2w, 2w+1, lane = row
+        {
+            const bool valid = r0 + lane < r_end && S.ptr[buf][lane] != nullptr;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int h = warp * 2 + hh;
+                const float x = valid ? (S.s[0][h][lane] + S.s[1][h][lane]) * A.scale_log2 : -INFINITY;
+                float mx = x;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float m_old = S.m[h];
+                const float m_new = fmaxf(m_old, mx);
+                const float p = (x == -INFINITY) ? 0.f : exp2f(x - m_new);
+                float sum = p;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+                const __nv_bfloat16 p_hi = __float2bfloat16_rn(p);
+                S.p[0][h][lane] = p_hi;
+                S.p[1][h][lane] = __float2bfloat16_rn(p - __bfloat162float(p_hi));
+                __syncwarp();
+                if (lane == 0) {
+                    S.l[h] = S.l[h] * alpha + sum;
+                    S.m[h] = m_new;
+                    S.alpha[h] = alpha;
+                }
             }
         }
         __syncthreads();
 
-        // ---- online softmax: warp w owns heads 4w..4w+3, lane = row
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
-            const int h = warp * 4 + hh;
-            const float x = S.s[h][lane];
-            float mx = x;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_old = S.m[h];
-            const float m_new = fmaxf(m_old, mx);
-            const float p = (x == -INFINITY) ? 0.f : exp2f(x - m_new);
-            float sum = p;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
-            const __nv_bfloat16 p_hi = __float2bfloat16_rn(p);
-            S.p[0][h][lane] = p_hi;
-            S.p[1][h][lane] = __float2bfloat16_rn(p - __bfloat162float(p_hi));
-            __syncwarp();
-            if (lane == 0) {
-                S.l[h] = S.l[h] * alpha + sum;
-                S.m[h] = m_new;
-                S.alpha[h] = alpha;
-            }
-        }
-        __syncthreads();
-
-        // ---- O = alpha O + P V: warp w owns columns 128w .. 128w+127
+        // ---- O = alpha O + P V: warp w owns columns 64w .. 64w+63
         {
             const float al0 = S.alpha[g], al1 = S.alpha[g + 8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 o[i][0] *= al0;
                 o[i][1] *= al0;
                 o[i][2] *= al1;
@@ -350,8 +492,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
                 ldsm_x4(pa + kPLoOffset, l0, l1, l2, l3);
                 const int vr = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-                for (int np = 0; np < 8; ++np) {
-                    const int chunk = (warp * 128 + np * 16) / 8 + (lane >> 4);
+                for (int np = 0; np < 4; ++np) {
+                    const int chunk = (warp * 64 + np * 16) / 8 + (lane >> 4);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_trans(rows_base + swz(vr, chunk), b0, b1, b2, b3);
                     mma_bf16_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
@@ -364,55 +506,80 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
         __syncthreads();
     }
 
-    // ---- write
-    if (A.splits == 1) {
+    // ---- write: the fragments go through shared memory (rows[0], free now:
+    // the last chunk's copies were waited for and its PV is done), 16-byte
+    // chunks of each head's 512 floats xor-swizzled by head, and leave as
+    // contiguous 16-byte stores (one head row of 2 KiB per 4 warp stores)
+    float sc0 = 1.f, sc1 = 1.f;
+    if (A.splits == 1 && A.cluster == 1) {
         float z0 = S.l[g], z1 = S.l[g + 8];
         if (A.sinks) {
             z0 += exp2f(A.sinks[h0 + g] * kLog2e - S.m[g]);
             z1 += exp2f(A.sinks[h0 + g + 8] * kLog2e - S.m[g + 8]);
         }
-        const float inv0 = z0 > 0.f ? 1.f / z0 : 0.f, inv1 = z1 > 0.f ? 1.f / z1 : 0.f;
-        float *o0 = A.out + (static_cast<int64_t>(t) * A.H + h0 + g) * kHD + warp * 128 + 2 * c;
-        float *o1 = o0 + 8 * kHD;
+        sc0 = z0 > 0.f ? 1.f / z0 : 0.f;
+        sc1 = z1 > 0.f ? 1.f / z1 : 0.f;
+    }
+    float *stg = reinterpret_cast<float *>(S.rows[0]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            *reinterpret_cast<float2 *>(o0 + i * 8) = make_float2(o[i][0] * inv0, o[i][1] * inv0);
-            *reinterpret_cast<float2 *>(o1 + i * 8) = make_float2(o[i][2] * inv1, o[i][3] * inv1);
-        }
-    } else {
-        const int64_t pbase = (static_cast<int64_t>(t) * A.splits + split) * A.H + h0;
-        float *o0 = A.part_o + (pbase + g) * kHD + warp * 128 + 2 * c;
-        float *o1 = o0 + 8 * kHD;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            *reinterpret_cast<float2 *>(o0 + i * 8) = make_float2(o[i][0], o[i][1]);
-            *reinterpret_cast<float2 *>(o1 + i * 8) = make_float2(o[i][2], o[i][3]);
-        }
-        if (threadIdx.x < kHeadGroup) {
-            A.part_ml[(pbase + threadIdx.x) * 2 + 0] = S.m[threadIdx.x];
-            A.part_ml[(pbase + threadIdx.x) * 2 + 1] = S.l[threadIdx.x];
+    for (int i = 0; i < 8; ++i) {
+        const int col = warp * 64 + i * 8 + 2 * c;
+        const int ch = col >> 2, wi = col & 3;
+        *reinterpret_cast<float2 *>(stg + g * kHD + ((ch ^ (g & 7)) << 2) + wi) =
+            make_float2(o[i][0] * sc0, o[i][1] * sc0);
+        *reinterpret_cast<float2 *>(stg + (g + 8) * kHD + ((ch ^ (g & 7)) << 2) + wi) =
+            make_float2(o[i][2] * sc1, o[i][3] * sc1);
+    }
+    if (A.cluster > 1) {
+        __syncthreads();
+        cluster_merge(A, S, t, split, h0, bad);
+        return;
+    }
+    const int64_t pbase = (static_cast<int64_t>(t) * A.splits + split) * A.H + h0;
+    if (A.splits > 1 && threadIdx.x < kHeadGroup) {
+        A.part_ml[(pbase + threadIdx.x) * 2 + 0] = S.m[threadIdx.x];
+        A.part_ml[(pbase + threadIdx.x) * 2 + 1] = S.l[threadIdx.x];
+    }
+    __syncthreads();
+    float *dst = A.splits == 1 ? A.out + (static_cast<int64_t>(t) * A.H + h0) * kHD
+                               : A.part_o + pbase * kHD;
+    const bool vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+    for (int e = threadIdx.x; e < kHeadGroup * (kHD / 4); e += kAttnThreads) {
+        const int h = e / (kHD / 4), ch = e % (kHD / 4);
+        const float4 v = *reinterpret_cast<const float4 *>(stg + h * kHD + ((ch ^ (h & 7)) << 2));
+        float *d = dst + h * kHD + ch * 4;
+        if (vec) {
+            *reinterpret_cast<float4 *>(d) = v;
+        } else {
+            d[0] = v.x;
+            d[1] = v.y;
+            d[2] = v.z;
+            d[3] = v.w;
         }
     }
     raise_status(A.status, bad);
 }
 
 // out[t,h,:] = sum_s 2^(m_s - M) O_s / (sum_s 2^(m_s - M) l_s [+ 2^(sink*log2e - M)])
-__global__ void __launch_bounds__(256) combine_kernel(const AttnParams A) {
+// Runs only when a token's splits span more than one cluster, and then the
+// plan makes every cluster a single CTA: one partial per split.
+__global__ void __launch_bounds__(64) combine_kernel(const AttnParams A) {
     pdl_wait();
     pdl_launch_dependents();
     const int h = blockIdx.x, t = blockIdx.y;
+    const int c0 = blockIdx.z * (kHD / kCombineParts);   // this CTA's 128 columns
     __shared__ float wgt[64];
     __shared__ float inv_z;
     const TokRows tr = token_rows(A.R, t);
     const int nsp = min(A.splits, (tr.len + A.rows_split - 1) / A.rows_split);
     float *o = A.out + (static_cast<int64_t>(t) * A.H + h) * kHD;
     if (nsp <= 0) {
-        for (int i = threadIdx.x; i < kHD; i += blockDim.x) o[i] = 0.f;
+        for (int i = threadIdx.x; i < kHD / kCombineParts; i += blockDim.x) o[c0 + i] = 0.f;
         return;
     }
     // Issue every partial load first (they do not depend on the weights),
     // then the (m, l) of each split, then combine: one round trip.
-    const int d = threadIdx.x * 2;   // 256 threads x 2 columns
+    const int d = c0 + threadIdx.x * 2;   // 64 threads x 2 columns
     const float *pb = A.part_o + (static_cast<int64_t>(t) * A.splits * A.H + h) * kHD + d;
     const int64_t pstride = static_cast<int64_t>(A.H) * kHD;
     float2 v[kMaxSplits];
@@ -487,6 +654,7 @@ cudaError_t launch_attention(const Launch &lc, const RowSource &src, int32_t T,
     A.H = p.n_heads;
     A.splits = plan.splits;
     A.rows_split = plan.rows_split;
+    A.cluster = plan.attn_cluster;
     A.scale_log2 = p.scale * kLog2e;
     A.q = static_cast<const __nv_bfloat16 *>(q);
     A.sinks = sinks;
@@ -499,11 +667,13 @@ cudaError_t launch_attention(const Launch &lc, const RowSource &src, int32_t T,
     cudaError_t e = set_kernel_smem(attention_kernel, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.splits, p.n_heads / kHeadGroup, T);
-    e = launch_pdl(attention_kernel, grid, dim3(kAttnThreads), smem, lc.stream, A);
-    if (e != cudaSuccess || plan.splits == 1) return e;
+    e = launch_pdl_cluster(attention_kernel, grid, dim3(kAttnThreads), smem, lc.stream,
+                           plan.attn_cluster, A);
+    if (e != cudaSuccess || plan.splits == plan.attn_cluster) return e;
     e = set_kernel_smem(combine_kernel, 0);
     if (e != cudaSuccess) return e;
-    return launch_pdl(combine_kernel, dim3(p.n_heads, T), dim3(256), 0, lc.stream, A);
+    return launch_pdl(combine_kernel, dim3(p.n_heads, T, kCombineParts), dim3(64), 0, lc.stream,
+                      A);
 }
 
 }  // namespace csa

@@ -29,6 +29,8 @@ struct WsPlan {
     int32_t topk_per_tok = 1;  // top-k filter CTAs per token (1: one CTA owns the row)
     int32_t splits = 1;      // attention splits per token
     int32_t rows_split = 0;  // rows per attention split (multiple of kAttnChunk)
+    int32_t attn_cluster = 1;  // attention CTAs per thread-block cluster along the splits
+                               // (divides splits): they merge their partials on chip
     // Layout: [per-token state | ... free ... | data].  The state slots sit at
     // the front at offsets that depend only on the token index; the data
     // regions are packed against the end of the caller's workspace, so no
@@ -116,6 +118,28 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Programmatic dependent launch of a grid in clusters of cluster_x CTAs
+// along x (cluster_x == 1: a plain launch_pdl).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, int cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster_x > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
