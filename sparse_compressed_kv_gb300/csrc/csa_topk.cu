@@ -31,6 +31,8 @@ constexpr int kSelThreads = 512;
 constexpr int kStageCap = 8192;        // entries staged in shared memory (64 KiB)
 static_assert(kStageCap % (kSelThreads / 32) == 0, "per-warp staging runs");
 constexpr int kMaxPerThread = kMaxFilterChunk / kSelThreads;
+static_assert(kD2Bins == 4 * kSelThreads, "the resolver holds four digit-2 bins per thread");
+
 // Resolver: the first kSpec entries of each of the first kSpecSlots slots (one
 // 128-byte line, the part a filter CTA has just written) are read together
 // with the slot counts, kSpecThreads threads per slot.
@@ -58,39 +60,74 @@ struct SelectParams {
 
 // ---------------------------------------------------------------- helpers
 
-// Block-wide exclusive scan of one value per thread (32- or 64-bit).
-template <typename U>
-__device__ __forceinline__ U block_excl_scan(U v, U *warp_tmp, U *total) {
+// Block-wide exclusive scan of one value per thread, with one barrier: each
+// warp scans its lanes and publishes its total in buf[warp]; after the
+// barrier every warp reads all totals (a lane each) and sums those of the
+// warps before its own in one warp reduction.  The reads of buf come after
+// the barrier, so two scans with no barrier between them must use different
+// buffers.  Thread 0 gets the block total in *total.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *buf, uint32_t *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    U incl = v;
+    uint32_t incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        U y = __shfl_up_sync(0xffffffffu, incl, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
-    if (lane == 31) warp_tmp[warp] = incl;
+    if (lane == 31) buf[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        U x = lane < nw ? warp_tmp[lane] : U(0);
-        U xi = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            U y = __shfl_up_sync(0xffffffffu, xi, o);
-            if (lane >= o) xi += y;
-        }
-        if (lane < nw) warp_tmp[lane] = xi - x;
-        if (lane == nw - 1 && total) *total = xi;
+    const int nw = blockDim.x >> 5;
+    const uint32_t x = lane < nw ? buf[lane] : 0u;
+    const uint32_t before = __reduce_add_sync(0xffffffffu, lane < warp ? x : 0u);
+    if (total && warp == 0) {
+        const uint32_t all = __reduce_add_sync(0xffffffffu, x);
+        if (lane == 0) *total = all;
     }
+    return before + incl - v;
+}
+
+// Exclusive block scan of three counters packed in one 64-bit word: bits
+// 42..63, 22..41 and 0..21, each of whose block totals fits its field (so no
+// field carries into the next).  The warps scan the packed word; the sums of
+// the warp totals before each warp are three 32-bit warp reductions.  One
+// barrier; thread 0 gets the block total in *total.
+constexpr int kPackA = 42, kPackB = 22;
+constexpr uint32_t kMaskB = (1u << (kPackA - kPackB)) - 1u, kMaskC = (1u << kPackB) - 1u;
+// every field's block total is at most the entries of one token's slots
+static_assert(static_cast<int64_t>(kMaxPerTok) * kMaxFilterChunk <= kMaskC &&
+                  static_cast<int64_t>(kMaxPerTok) * kMaxFilterChunk / 8 + kMaxPerTok <= kMaskB &&
+                  kMaxPerTok <= kSelThreads,
+              "packed resolver scan fields");
+__device__ __forceinline__ uint64_t block_excl_scan3(uint64_t v, uint64_t *buf, uint64_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) buf[warp] = incl;
     __syncthreads();
-    U r = warp_tmp[warp] + incl - v;
-    __syncthreads();
-    return r;
+    const int nw = blockDim.x >> 5;
+    const uint64_t x = lane < nw ? buf[lane] : 0ull;
+    auto sum3 = [](uint64_t y) {
+        const uint32_t a = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(y >> kPackA));
+        const uint32_t b = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(y >> kPackB) & kMaskB);
+        const uint32_t c = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(y) & kMaskC);
+        return (static_cast<uint64_t>(a) << kPackA) | (static_cast<uint64_t>(b) << kPackB) | c;
+    };
+    const uint64_t before = sum3(lane < warp ? x : 0ull);
+    if (total && warp == 0) {
+        const uint64_t all = sum3(x);
+        if (lane == 0) *total = all;
+    }
+    return before + incl - v;
 }
 
 // Given a histogram h[0..nbins) and a rank k >= 1 counted from the top,
 // find the digit d with count(> d) < k <= count(>= d).  Writes d and
-// count(> d).  nbins is a multiple of blockDim.x.
+// count(> d).  nbins is a multiple of blockDim.x.  Ends with a barrier after
+// its last read of warp_tmp.
 __device__ void find_threshold_digit(const uint32_t *h, int nbins, uint32_t k, uint32_t *warp_tmp,
                                      int32_t *d_out, uint32_t *gt_out) {
     const int per = nbins / blockDim.x;
@@ -98,7 +135,7 @@ __device__ void find_threshold_digit(const uint32_t *h, int nbins, uint32_t k, u
     const int hi = nbins - threadIdx.x * per;
     uint32_t local = 0;
     for (int b = hi - 1; b >= hi - per; --b) local += h[b];
-    uint32_t above = block_excl_scan<uint32_t>(local, warp_tmp, nullptr);  // count in bins >= hi
+    uint32_t above = block_excl_scan(local, warp_tmp, nullptr);  // count in bins >= hi
     uint32_t run = above;
     for (int b = hi - 1; b >= hi - per; --b) {
         const uint32_t c = h[b];
@@ -150,8 +187,8 @@ __global__ void __launch_bounds__(256) score_hist_kernel(const SelectParams P) {
 struct SelectSmem {
     uint32_t h[kD1Bins];           // digit-1 histogram, then digit-3 histogram
     uint32_t h2[kD2Bins];          // digit-2 histogram of the threshold bin
-    uint32_t warp_tmp[32];
-    uint64_t warp_tmp64[32];
+    uint32_t warp_tmp[2 * 32];     // block scans: per-warp totals, two buffers
+    uint64_t warp_tmp64[32];       // the one 64-bit scan
     uint64_t total64;
     uint64_t stage[kStageCap];     // entries (key << 32 | index), ascending index
     uint32_t prefix[kMaxPerTok + 1];
@@ -161,8 +198,10 @@ struct SelectSmem {
     uint32_t overflow;
     int32_t d;                     // threshold digit of the current pass
     uint32_t gt;                   // count strictly above the threshold digit
-    uint32_t total;
     uint32_t last;
+    uint32_t cand[32];             // keys sharing digits 1 and 2 with the k-th, when <= 32
+    uint32_t ncand;
+    uint32_t tau, need3, eq3;      // the k-th key, ties to take, ties in all
 };
 
 // Two CTAs per SM: the filter grid (about two CTAs per SM) runs in one wave.
@@ -340,6 +379,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
         const uint32_t d1 = static_cast<uint32_t>(S.d);
         uint32_t need = kk - S.gt;   // >= 1, all from digit-1 bin d1
         bool d2_found = false;
+        bool gathered = false;       // the digit-1/2 bin's keys were collected while staging
+        uint32_t pre22 = 0;
         if (!P.local_hist) {
             // One round trip: the slot counts, the digit-2 histogram and the
             // first kSpec entries of every slot, read before their counts are
@@ -347,44 +388,74 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
             const int pt = P.per_tok;
             const uint64_t *base = P.slots + static_cast<int64_t>(t) * pt * P.chunk;
             const uint32_t c = tid < pt ? __ldcg(&P.slot_cnt[static_cast<int64_t>(t) * pt + tid]) : 0u;
-            uint32_t h2r[kD2Bins / kSelThreads];
-#pragma unroll
-            for (int u = 0; u < kD2Bins / kSelThreads; ++u) h2r[u] = __ldcg(&gh2[u * kSelThreads + tid]);
+            // thread i holds digit-2 bins hb .. hb+3 (thread 0 the top four)
+            const int hb = kD2Bins - 4 * (tid + 1);
+            const uint4 h2v = __ldcg(reinterpret_cast<const uint4 *>(gh2 + hb));
             const int ssl = tid / kSpecThreads;                     // slot of this thread's guess
             const uint32_t se0 = (tid % kSpecThreads) * kSpecPer;  // its first entry
             uint64_t sv[kSpecPer];
 #pragma unroll
             for (int u = 0; u < kSpecPer; ++u)
                 sv[u] = ssl < pt ? __ldcg(base + static_cast<int64_t>(ssl) * P.chunk + se0 + u) : 0ull;
-#pragma unroll
-            for (int u = 0; u < kD2Bins / kSelThreads; ++u) S.h2[u * kSelThreads + tid] = h2r[u];
-            // entry offsets, and offsets of the groups of up to 8 entries the
-            // guesses did not cover, in one packed scan
+            *reinterpret_cast<uint4 *>(&S.h2[hb]) = h2v;
+            // One scan gives the entry offsets, the offsets of the groups of
+            // up to 8 entries the guesses did not cover, and the digit-2
+            // counts above each thread's bins.
             const uint32_t spec = tid < pt && tid < kSpecSlots ? min(c, static_cast<uint32_t>(kSpec)) : 0u;
-            const uint64_t packed = (static_cast<uint64_t>((c - spec + 7) / 8) << 32) | c;
-            const uint64_t off = block_excl_scan<uint64_t>(packed, S.warp_tmp64, &S.total64);
+            const uint64_t packed = (static_cast<uint64_t>(c) << kPackA) |
+                                    (static_cast<uint64_t>((c - spec + 7) / 8) << kPackB) |
+                                    (h2v.x + h2v.y + h2v.z + h2v.w);
+            const uint64_t off = block_excl_scan3(packed, S.warp_tmp64, &S.total64);
             if (tid < pt) {
-                S.prefix[tid] = static_cast<uint32_t>(off);
-                S.gprefix[tid] = static_cast<uint32_t>(off >> 32);
+                S.prefix[tid] = static_cast<uint32_t>(off >> kPackA);
+                S.gprefix[tid] = static_cast<uint32_t>(off >> kPackB) & kMaskB;
+            }
+            {
+                // digit 2: the bin where the count from the top reaches need
+                uint32_t run = static_cast<uint32_t>(off) & kMaskC;
+                const uint32_t hv[4] = {h2v.w, h2v.z, h2v.y, h2v.x};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (run < need && run + hv[j] >= need) {
+                        S.d = hb + 3 - j;
+                        S.gt = run;
+                    }
+                    run += hv[j];
+                }
             }
             if (tid == 0) {
                 const uint64_t tot = S.total64;
-                S.prefix[pt] = static_cast<uint32_t>(tot);
-                S.gprefix[pt] = static_cast<uint32_t>(tot >> 32);
-                S.nstage = static_cast<uint32_t>(tot);
-                S.overflow = (tot & 0xffffffffull) > static_cast<uint64_t>(kStageCap);
+                S.prefix[pt] = static_cast<uint32_t>(tot >> kPackA);
+                S.gprefix[pt] = static_cast<uint32_t>(tot >> kPackB) & kMaskB;
+                S.nstage = static_cast<uint32_t>(tot >> kPackA);
+                S.overflow = (tot >> kPackA) > static_cast<uint64_t>(kStageCap);
+                S.ncand = 0;
             }
             __syncthreads();
-            // digit 2 needs only the histogram: find it now
-            find_threshold_digit(S.h2, kD2Bins, need, S.warp_tmp, &S.d, &S.gt);
             d2_found = true;
+            need -= S.gt;
+            pre22 = (d1 << kD2Bits) | static_cast<uint32_t>(S.d);
+            // The entries sharing digits 1 and 2 with the k-th key number
+            // h2[d2]; when they fit one warp their keys are collected as the
+            // entries are staged, and one warp finds the k-th key among them.
+            gathered = !S.overflow && S.h2[S.d] <= 32u;
+            auto collect = [&](uint64_t e) {
+                const uint32_t key = static_cast<uint32_t>(e >> 32);
+                if ((key >> kD2Shift) == pre22) {
+                    const uint32_t at = atomicAdd(&S.ncand, 1u);
+                    if (at < 32u) S.cand[at] = key;
+                }
+            };
             if (!S.overflow) {
                 if (ssl < pt && ssl < kSpecSlots) {
                     const uint32_t cnt = S.prefix[ssl + 1] - S.prefix[ssl];
                     uint64_t *dst = S.stage + S.prefix[ssl];
 #pragma unroll
                     for (int u = 0; u < kSpecPer; ++u)
-                        if (se0 + u < cnt) dst[se0 + u] = sv[u];
+                        if (se0 + u < cnt) {
+                            dst[se0 + u] = sv[u];
+                            if (gathered) collect(sv[u]);
+                        }
                 }
                 // the rest: one group per thread, its slot by one search over
                 // the group offsets, up to eight independent loads in flight
@@ -406,7 +477,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                     for (int u = 0; u < 8; ++u) val[u] = e0 + u < cnt ? __ldcg(src + u) : 0ull;
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
-                        if (e0 + u < cnt) dst[u] = val[u];
+                        if (e0 + u < cnt) {
+                            dst[u] = val[u];
+                            if (gathered) collect(val[u]);
+                        }
                 }
             }
         }
@@ -425,24 +499,61 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                 index = i;
             }
         };
-        // ---- digit 2 from its histogram, then digit 3 over the few entries
-        // that share digits 1 and 2
-        if (!d2_found) find_threshold_digit(S.h2, kD2Bins, need, S.warp_tmp, &S.d, &S.gt);
-        need -= S.gt;
-        const uint32_t pre22 = (d1 << kD2Bits) | static_cast<uint32_t>(S.d);
-        for (int i = tid; i < kD1Bins; i += blockDim.x) S.h[i] = 0;
-        __syncthreads();
-        for (int64_t i = tid; i < m; i += blockDim.x) {
-            uint32_t key;
-            int64_t index;
-            entry(i, key, index);
-            if ((key >> kD2Shift) == pre22) atomicAdd(&S.h[key & (kD3Bins - 1)], 1u);
+        // ---- the k-th key tau: the need-th largest of the entries that
+        // share digits 1 and 2 with it
+        uint32_t tau, eq;
+        if (gathered) {
+            // one warp, a key per lane: its rank among the collected keys
+            if (warp == 0) {
+                const uint32_t nc = min(S.ncand, 32u);
+                const uint32_t key = static_cast<uint32_t>(lane) < nc ? S.cand[lane] : 0u;
+                uint32_t above = 0, same = 0;
+                // rolled: this code runs once per launch, and every
+                // instruction of it is fetched cold
+#pragma unroll 1
+                for (uint32_t j = 0; j < nc; ++j) {
+                    const uint32_t o = __shfl_sync(0xffffffffu, key, static_cast<int>(j));
+                    above += o > key ? 1u : 0u;
+                    same += o == key ? 1u : 0u;
+                }
+                const bool hit = static_cast<uint32_t>(lane) < nc && above < need && need <= above + same;
+                const unsigned hm = __ballot_sync(0xffffffffu, hit);
+                const int src = hm ? __ffs(hm) - 1 : 0;
+                const uint32_t tk = __shfl_sync(0xffffffffu, key, src);
+                const uint32_t ta = __shfl_sync(0xffffffffu, above, src);
+                const uint32_t ts = __shfl_sync(0xffffffffu, same, src);
+                if (lane == 0) {
+                    S.tau = tk;
+                    S.need3 = need - ta;
+                    S.eq3 = ts;
+                }
+            }
+            __syncthreads();
+            tau = S.tau;
+            need = S.need3;
+            eq = S.eq3;
+        } else {
+            // digit 2 from its histogram (if not found yet), then digit 3
+            // over the entries that share digits 1 and 2
+            if (!d2_found) {
+                find_threshold_digit(S.h2, kD2Bins, need, S.warp_tmp, &S.d, &S.gt);
+                need -= S.gt;
+                pre22 = (d1 << kD2Bits) | static_cast<uint32_t>(S.d);
+            }
+            for (int i = tid; i < kD3Bins; i += blockDim.x) S.h[i] = 0;
+            __syncthreads();
+            for (int64_t i = tid; i < m; i += blockDim.x) {
+                uint32_t key;
+                int64_t index;
+                entry(i, key, index);
+                if ((key >> kD2Shift) == pre22) atomicAdd(&S.h[key & (kD3Bins - 1)], 1u);
+            }
+            __syncthreads();
+            find_threshold_digit(S.h, kD3Bins, need, S.warp_tmp, &S.d, &S.gt);
+            need -= S.gt;
+            tau = (pre22 << kD2Shift) | static_cast<uint32_t>(S.d);
+            eq = S.h[S.d];
         }
-        __syncthreads();
-        find_threshold_digit(S.h, kD1Bins, need, S.warp_tmp, &S.d, &S.gt);
-        need -= S.gt;
-        const uint32_t tau = (pre22 << kD2Shift) | static_cast<uint32_t>(S.d);
-        const uint32_t eq = S.h[S.d];
         // ---- ordered compaction: every key above tau, then the `need`
         // lowest-index keys equal to tau; thread-contiguous runs keep order
         const int64_t run = (m + blockDim.x - 1) / blockDim.x;
@@ -456,7 +567,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                 entry(i, key, index);
                 ties += key == tau ? 1u : 0u;
             }
-            tie_before = block_excl_scan<uint32_t>(ties, S.warp_tmp, &S.total);
+            tie_before = block_excl_scan(ties, S.warp_tmp, nullptr);
         }
         const bool all_ties = need == eq;
         uint32_t take_n = 0;
@@ -471,7 +582,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                 tb += is_tie ? 1u : 0u;
             }
         }
-        uint32_t pos = block_excl_scan<uint32_t>(take_n, S.warp_tmp, &S.total);
+        uint32_t taken = 0;
+        // no barrier since the tie scan: the other buffer
+        uint32_t pos = block_excl_scan(take_n, S.warp_tmp + 32, &taken);
         {
             uint32_t tb = tie_before;
             for (int64_t i = r0; i < r1; ++i) {
@@ -487,7 +600,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
             }
         }
         for (int i = kk + tid; i < P.top_k; i += blockDim.x) out[i] = -1;
-        if (S.total != kk && tid == 0) raise_status(P.status, CSA_DEV_BAD_INDEX);
+        if (taken != kk && tid == 0) raise_status(P.status, CSA_DEV_BAD_INDEX);
     }
     if (tid == 0) P.nsel_out[t] = static_cast<int32_t>(kk);
     // ---- leave the per-token state zeroed for the next call (in one-CTA mode
