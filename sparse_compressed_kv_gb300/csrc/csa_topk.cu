@@ -35,11 +35,12 @@ static_assert(kD2Bins == 4 * kSelThreads, "the resolver holds four digit-2 bins 
 
 // Resolver: the first kSpec entries of each of the first kSpecSlots slots (one
 // 128-byte line, the part a filter CTA has just written) are read together
-// with the slot counts, kSpecThreads threads per slot.
-constexpr int kSpecPer = 8;
-constexpr int kSpecThreads = 2;
-constexpr int kSpec = kSpecPer * kSpecThreads;
-constexpr int kSpecSlots = kSelThreads / kSpecThreads;
+// with the slot counts: 16 bytes (two entries) per thread, eight threads per
+// line, so each warp load covers four whole lines.
+constexpr int kSpec = 16;
+constexpr int kSpecLanes = kSpec / 2;                      // threads per slot line
+constexpr int kSpecRounds = 4;                             // lines per thread
+constexpr int kSpecSlots = kSelThreads / kSpecLanes * kSpecRounds;   // 256
 
 struct SelectParams {
     csa_layout_t L;
@@ -391,12 +392,18 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
             // thread i holds digit-2 bins hb .. hb+3 (thread 0 the top four)
             const int hb = kD2Bins - 4 * (tid + 1);
             const uint4 h2v = __ldcg(reinterpret_cast<const uint4 *>(gh2 + hb));
-            const int ssl = tid / kSpecThreads;                     // slot of this thread's guess
-            const uint32_t se0 = (tid % kSpecThreads) * kSpecPer;  // its first entry
-            uint64_t sv[kSpecPer];
+            // entries se0, se0 + 1 of slots ssl0 + u * kSpecStride
+            constexpr int kSpecStride = kSelThreads / kSpecLanes;
+            const int ssl0 = tid / kSpecLanes;
+            const uint32_t se0 = (tid % kSpecLanes) * 2;
+            ulonglong2 sv[kSpecRounds];
 #pragma unroll
-            for (int u = 0; u < kSpecPer; ++u)
-                sv[u] = ssl < pt ? __ldcg(base + static_cast<int64_t>(ssl) * P.chunk + se0 + u) : 0ull;
+            for (int u = 0; u < kSpecRounds; ++u) {
+                const int sl = ssl0 + u * kSpecStride;
+                sv[u] = sl < pt ? __ldcg(reinterpret_cast<const ulonglong2 *>(
+                                      base + static_cast<int64_t>(sl) * P.chunk + se0))
+                                : make_ulonglong2(0ull, 0ull);
+            }
             *reinterpret_cast<uint4 *>(&S.h2[hb]) = h2v;
             // One scan gives the entry offsets, the offsets of the groups of
             // up to 8 entries the guesses did not cover, and the digit-2
@@ -447,15 +454,21 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                 }
             };
             if (!S.overflow) {
-                if (ssl < pt && ssl < kSpecSlots) {
-                    const uint32_t cnt = S.prefix[ssl + 1] - S.prefix[ssl];
-                    uint64_t *dst = S.stage + S.prefix[ssl];
 #pragma unroll
-                    for (int u = 0; u < kSpecPer; ++u)
-                        if (se0 + u < cnt) {
-                            dst[se0 + u] = sv[u];
-                            if (gathered) collect(sv[u]);
+                for (int u = 0; u < kSpecRounds; ++u) {
+                    const int sl = ssl0 + u * kSpecStride;
+                    if (sl < pt) {
+                        const uint32_t cnt = S.prefix[sl + 1] - S.prefix[sl];
+                        uint64_t *dst = S.stage + S.prefix[sl];
+                        if (se0 < cnt) {
+                            dst[se0] = sv[u].x;
+                            if (gathered) collect(sv[u].x);
                         }
+                        if (se0 + 1 < cnt) {
+                            dst[se0 + 1] = sv[u].y;
+                            if (gathered) collect(sv[u].y);
+                        }
+                    }
                 }
                 // the rest: one group per thread, its slot by one search over
                 // the group offsets, up to eight independent loads in flight
