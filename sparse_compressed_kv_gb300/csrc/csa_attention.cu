@@ -327,8 +327,7 @@ __device__ __forceinline__ void cluster_merge(const AttnParams &A, AttnSmem &S, 
 
 __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParams A) {
     extern __shared__ uint8_t smem_raw[];
-    AttnSmem &S = *reinterpret_cast<AttnSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    AttnSmem &S = *reinterpret_cast<AttnSmem *>(align_smem<128>(smem_raw));
     const int split = blockIdx.x, hg = blockIdx.y, t = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;

@@ -61,13 +61,23 @@ __device__ __forceinline__ TokenView token_view(const csa_layout_t &L, int ratio
     v.off = 0;
     v.n_vis = 0;
     v.bad = 0;
+    // The sequence's offsets depend on its id.  Token t usually belongs to
+    // sequence min(t, num_seqs - 1) (one token per sequence in a decode
+    // batch, one sequence in a prefill chunk): its offsets are loaded in the
+    // same round trip as the id and reloaded only when the guess is wrong.
+    const int g = t < L.num_seqs ? t : L.num_seqs - 1;
+    const int gs = g > 0 ? g : 0;
     int b = L.tok_seq[t];
     int64_t p = L.tok_pos[t];
+    int64_t o0 = L.comp_off[gs], o1 = L.comp_off[gs + 1];
     if (b < 0 || b >= L.num_seqs || p < 0) {
         v.bad = CSA_DEV_BAD_LAYOUT;
         return v;
     }
-    int64_t o0 = L.comp_off[b], o1 = L.comp_off[b + 1];
+    if (b != gs) {
+        o0 = L.comp_off[b];
+        o1 = L.comp_off[b + 1];
+    }
     if (o0 < 0 || o1 < o0 || o1 > L.total_comp_rows) {
         v.bad = CSA_DEV_BAD_LAYOUT;
         return v;
@@ -107,6 +117,16 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// The dynamic shared-memory array rounded up to an A-byte boundary.  The
+// padding is added to the array's own pointer (not through an integer), so
+// the compiler still sees a shared-memory address and emits shared loads and
+// stores for what is reached through it.
+template <uint32_t A>
+__device__ __forceinline__ uint8_t *align_smem(uint8_t *base) {
+    const uint32_t s = smem_addr(base);
+    return base + (((s + (A - 1u)) & ~(A - 1u)) - s);
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }

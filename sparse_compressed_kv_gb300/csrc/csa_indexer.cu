@@ -125,8 +125,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp4>::kThreads, 1)
                    const IndexerParams P) {
     using C = IdxCfg<G, kFp4>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = align_smem<1024>(smem_raw);
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::kStages * C::kABytes;
     uint8_t *sF = sB + C::kBBytes;  // FP4 key ring (FP4 only)

@@ -125,26 +125,40 @@ __device__ __forceinline__ uint64_t block_excl_scan3(uint64_t v, uint64_t *buf, 
     return before + incl - v;
 }
 
-// Given a histogram h[0..nbins) and a rank k >= 1 counted from the top,
-// find the digit d with count(> d) < k <= count(>= d).  Writes d and
-// count(> d).  nbins is a multiple of blockDim.x.  Ends with a barrier after
-// its last read of warp_tmp.
-__device__ void find_threshold_digit(const uint32_t *h, int nbins, uint32_t k, uint32_t *warp_tmp,
-                                     int32_t *d_out, uint32_t *gt_out) {
-    const int per = nbins / blockDim.x;
-    // thread i owns bins [nbins - (i+1)*per, nbins - i*per): thread 0 owns the top bins
-    const int hi = nbins - threadIdx.x * per;
+// Given a histogram h[0..kBins) in shared memory and a rank k >= 1 counted
+// from the top, find the digit d with count(> d) < k <= count(>= d).  Writes
+// d and count(> d).  Thread i holds the kBins / kSelThreads bins just below
+// kBins - i * per (thread 0 the top ones), read as one vector.  Ends with a
+// barrier after its last read of warp_tmp.
+template <int kBins>
+__device__ __forceinline__ void find_threshold_digit(const uint32_t *h, uint32_t k, uint32_t *warp_tmp,
+                                                     int32_t *d_out, uint32_t *gt_out) {
+    constexpr int per = kBins / kSelThreads;
+    static_assert(kBins % kSelThreads == 0 && (per == 2 || per == 4), "bins per thread");
+    const int hb = per * (kSelThreads - 1 - static_cast<int>(threadIdx.x));
+    uint32_t v[per];
+    if constexpr (per == 4) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(h + hb);
+        v[0] = q.x;
+        v[1] = q.y;
+        v[2] = q.z;
+        v[3] = q.w;
+    } else {
+        const uint2 q = *reinterpret_cast<const uint2 *>(h + hb);
+        v[0] = q.x;
+        v[1] = q.y;
+    }
     uint32_t local = 0;
-    for (int b = hi - 1; b >= hi - per; --b) local += h[b];
-    uint32_t above = block_excl_scan(local, warp_tmp, nullptr);  // count in bins >= hi
-    uint32_t run = above;
-    for (int b = hi - 1; b >= hi - per; --b) {
-        const uint32_t c = h[b];
-        if (run < k && run + c >= k) {
-            *d_out = b;
+#pragma unroll
+    for (int j = 0; j < per; ++j) local += v[j];
+    uint32_t run = block_excl_scan(local, warp_tmp, nullptr);  // count in bins above hb + per - 1
+#pragma unroll
+    for (int j = per - 1; j >= 0; --j) {
+        if (run < k && run + v[j] >= k) {
+            *d_out = hb + j;
             *gt_out = run;
         }
-        run += c;
+        run += v[j];
     }
     __syncthreads();
 }
@@ -208,8 +222,7 @@ struct SelectSmem {
 // Two CTAs per SM: the filter grid (about two CTAs per SM) runs in one wave.
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectParams P) {
     extern __shared__ uint8_t smem_raw[];
-    SelectSmem &S = *reinterpret_cast<SelectSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+    SelectSmem &S = *reinterpret_cast<SelectSmem *>(align_smem<16>(smem_raw));
     const int t = blockIdx.y;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -269,7 +282,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
             for (int u = 0; u < kD1Bins / kSelThreads; ++u) S.h[u * kSelThreads + tid] = hreg[u];
         }
         __syncthreads();
-        find_threshold_digit(S.h, kD1Bins, kk, S.warp_tmp, &S.d, &S.gt);
+        find_threshold_digit<kD1Bins>(S.h, kk, S.warp_tmp, &S.d, &S.gt);
         const uint32_t d1 = static_cast<uint32_t>(S.d);
 
         if (P.local_hist) {
@@ -549,7 +562,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
             // digit 2 from its histogram (if not found yet), then digit 3
             // over the entries that share digits 1 and 2
             if (!d2_found) {
-                find_threshold_digit(S.h2, kD2Bins, need, S.warp_tmp, &S.d, &S.gt);
+                find_threshold_digit<kD2Bins>(S.h2, need, S.warp_tmp, &S.d, &S.gt);
                 need -= S.gt;
                 pre22 = (d1 << kD2Bits) | static_cast<uint32_t>(S.d);
             }
@@ -562,7 +575,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                 if ((key >> kD2Shift) == pre22) atomicAdd(&S.h[key & (kD3Bins - 1)], 1u);
             }
             __syncthreads();
-            find_threshold_digit(S.h, kD3Bins, need, S.warp_tmp, &S.d, &S.gt);
+            find_threshold_digit<kD3Bins>(S.h, need, S.warp_tmp, &S.d, &S.gt);
             need -= S.gt;
             tau = (pre22 << kD2Shift) | static_cast<uint32_t>(S.d);
             eq = S.h[S.d];
