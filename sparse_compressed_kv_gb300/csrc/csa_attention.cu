@@ -569,8 +569,15 @@ __global__ void __launch_bounds__(64) combine_kernel(const AttnParams A) {
     const int c0 = blockIdx.z * (kHD / kCombineParts);   // this CTA's 128 columns
     __shared__ float wgt[64];
     __shared__ float inv_z;
-    const TokRows tr = token_rows(A.R, t);
-    const int nsp = min(A.splits, (tr.len + A.rows_split - 1) / A.rows_split);
+    __shared__ int nsp_s;
+    // one thread reads the token's record (every thread of every CTA
+    // reading the same lines would queue their requests) and shares it
+    if (threadIdx.x == 0) {
+        const TokRows tr = token_rows(A.R, t);
+        nsp_s = min(A.splits, (tr.len + A.rows_split - 1) / A.rows_split);
+    }
+    __syncthreads();
+    const int nsp = nsp_s;
     float *o = A.out + (static_cast<int64_t>(t) * A.H + h) * kHD;
     if (nsp <= 0) {
         for (int i = threadIdx.x; i < kHD / kCombineParts; i += blockDim.x) o[c0 + i] = 0.f;

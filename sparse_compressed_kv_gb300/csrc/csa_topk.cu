@@ -177,13 +177,14 @@ __device__ __forceinline__ void smem_hist_add(uint32_t *h, uint32_t bin, bool ac
 
 __global__ void __launch_bounds__(256) score_hist_kernel(const SelectParams P) {
     __shared__ uint32_t h[kD1Bins];
+    __shared__ int64_t n_vis;
     pdl_wait();
     pdl_launch_dependents();
     const int t = blockIdx.y;
     for (int i = threadIdx.x; i < kD1Bins; i += blockDim.x) h[i] = 0;
+    if (threadIdx.x == 0) n_vis = token_view(P.L, P.ratio, t).n_vis;   // one reader, shared
     __syncthreads();
-    const TokenView v = token_view(P.L, P.ratio, t);
-    const int64_t n = v.n_vis;
+    const int64_t n = n_vis;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * P.chunk;
     const int64_t b1 = min(n, b0 + P.chunk);
     const float *sc = P.scores + static_cast<int64_t>(t) * P.ld;
@@ -214,6 +215,7 @@ struct SelectSmem {
     int32_t d;                     // threshold digit of the current pass
     uint32_t gt;                   // count strictly above the threshold digit
     uint32_t last;
+    int64_t n_vis;                 // the token's visible blocks
     uint32_t cand[32];             // keys sharing digits 1 and 2 with the k-th, when <= 32
     uint32_t ncand;
     uint32_t tau, need3, eq3;      // the k-th key, ties to take, ties in all
@@ -258,9 +260,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
             keys[q] = (q * 32 < span && i < cend) ? score_key(__ldcg(row + i)) : 0u;
         }
     }
-    const TokenView v = token_view(P.L, P.ratio, t);
-    if (v.bad && blockIdx.x == 0 && tid == 0) raise_status(P.status, v.bad);
-    const int64_t n = v.n_vis;
+    // The token's record: one thread reads it (every thread of every CTA
+    // reading the same few lines would queue thousands of requests on them)
+    // and the barrier below shares it.
+    if (tid == 0) {
+        const TokenView v = token_view(P.L, P.ratio, t);
+        if (v.bad && blockIdx.x == 0) raise_status(P.status, v.bad);
+        S.n_vis = v.n_vis;
+    }
+    if (!P.local_hist)
+#pragma unroll
+        for (int u = 0; u < kD1Bins / kSelThreads; ++u) S.h[u * kSelThreads + tid] = hreg[u];
+    __syncthreads();
+    const int64_t n = S.n_vis;
     const uint32_t kk = static_cast<uint32_t>(min(static_cast<int64_t>(P.top_k), n));
     const float *sc = P.scores + static_cast<int64_t>(t) * P.ld;
     const bool rank = kk > 0 && kk < n;
@@ -277,11 +289,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                 const int64_t i = base + tid;
                 smem_hist_add(S.h, i < n ? score_key(__ldcg(&sc[i])) >> kD1Shift : 0u, i < n);
             }
-        } else {
-#pragma unroll
-            for (int u = 0; u < kD1Bins / kSelThreads; ++u) S.h[u * kSelThreads + tid] = hreg[u];
+            __syncthreads();
         }
-        __syncthreads();
         find_threshold_digit<kD1Bins>(S.h, kk, S.warp_tmp, &S.d, &S.gt);
         const uint32_t d1 = static_cast<uint32_t>(S.d);
 
