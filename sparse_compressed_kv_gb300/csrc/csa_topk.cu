@@ -385,13 +385,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
     if (!P.local_hist) {
         __syncthreads();
         if (tid == 0) {
-            __threadfence();
-            const uint32_t prev = atomicAdd(&cnt->ticket, 1u);
+            // release: every thread's slot writes (ordered before this by the
+            // barrier) are visible to whoever takes the last ticket; acquire:
+            // the last CTA then sees every other CTA's (the barrier below
+            // carries it to the other threads)
+            uint32_t prev;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                         : "=r"(prev)
+                         : "l"(&cnt->ticket)
+                         : "memory");
             S.last = (prev == gridDim.x - 1) ? 1u : 0u;
         }
         __syncthreads();
         if (!S.last) return;
-        __threadfence();
     }
 
     int32_t *out = P.idx_out + static_cast<int64_t>(t) * P.top_k;
