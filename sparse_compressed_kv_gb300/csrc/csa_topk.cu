@@ -14,12 +14,16 @@
 //                          and compacts, with a block-wide scan, the entries
 //                          (key, index) whose digit 1 is >= d1 into its own
 //                          output slot: no shared counters, no contention;
-//   resolve                the last CTA of the token (atomic ticket) stages
-//                          every slot's entries in shared memory in one round
-//                          trip; digit-1 winners are in, digits 2 and 3 over
-//                          the threshold bin give the exact k-th key; ties at
-//                          that key are taken in ascending index order; a
-//                          bitmap over the index range emits the set sorted.
+//   resolve                the last CTA of the token (atomic ticket) reads
+//                          the slot counts, the digit-2 histogram and every
+//                          slot's first line in one round trip and stages the
+//                          entries in shared memory in index order; digit-1
+//                          winners are in; digit 2 comes from its histogram,
+//                          and the few keys that share digits 1 and 2 with the
+//                          k-th are ranked by one warp (a digit-3 histogram
+//                          when they are more than 32), which gives the exact
+//                          k-th key; ties at that key are taken in ascending
+//                          index order; an ordered compaction emits the set.
 // The result is a pure function of the score bits.  The kernel that consumes
 // the per-token state (histogram, ticket) zeroes it for the next call.
 #include "csa_device.cuh"
