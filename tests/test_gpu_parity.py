@@ -159,8 +159,12 @@ def test_device_status_bits(cuda_device):
     assert run.dev_status() & csa.DEV_MISSING_SWA
 
 
-def test_sink_attention(cuda_device):
-    wl = W.tiny(seed=3)
+@pytest.mark.parametrize("name", ["tiny", "wide"])
+def test_sink_attention(cuda_device, name):
+    # tiny: 6 splits merged by one thread-block cluster; wide: 36 splits of
+    # 32 rows merged by the combine kernel (the sink in its denominator)
+    wl = W.tiny(seed=3) if name == "tiny" else W.make(
+        "sinkwide", seed=5, seq_lens=[4 * 5000], n_comp=[5000], top_k=1024, n_heads=16)
     run = H.Run(wl, cuda_device)
     sc = run.scores()
     idx, n_sel = run.topk(sc)
