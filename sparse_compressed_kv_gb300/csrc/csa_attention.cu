@@ -12,11 +12,14 @@
 // by index and from the window ring in fused mode, "1M-context viability",
 // M5), QK^T and PV run on mma.sync bf16 tensor-core tiles with f32
 // accumulation, and the softmax is online across chunks with warp-shuffle
-// reductions.  Each row is read once for all 16 heads of the CTA.  With more
-// than one split per token, the splits run in thread-block clusters of up to 8
-// neighbouring CTAs that merge their partial (m, l, O) through distributed
-// shared memory with log-sum-exp weights; when more than one cluster covers a
-// token, a combine kernel merges the clusters' partials the same way.
+// reductions.  Each row is read once for all 16 heads of the CTA.  With 2 to
+// 8 splits per token, the splits run as one thread-block cluster that merges
+// their partial (m, l, O) through distributed shared memory with log-sum-exp
+// weights and writes the output.  With more, each split writes its partial
+// to the workspace and a combine kernel merges them the same way.  (The merge
+// also handles clusters that cover part of a token, one partial per cluster;
+// the plan does not use that, as an on-chip merge of partials is no faster
+// than a pass through L2.)
 #include <math.h>
 
 #include "csa_device.cuh"
