@@ -133,7 +133,8 @@ class Layer:
 
 
 def algorithmic_bytes(wl: W.Workload):
-    """Bytes the method must move for one step (measurement)."""
+    """Bytes the method must move for one step: the visible indexer keys, the
+    selected and window rows, the token's activations and its f32 output."""
     keys = rows = 0
     T = wl.num_tokens
     for t in range(T):
@@ -215,26 +216,179 @@ def time_graphs(graphs, steps, warmup, stream):
     return t0.elapsed_time(t1) / steps
 
 
-def time_steps(group, singles, steps, warmup, stream):
-    """Time exactly `steps` steps: replays of `group` (one graph holding one
-    step per rotating layer, back to back as a model's layers are captured
-    together), then single-step graphs for the remainder.  CUDA events on
-    `stream`, which is made current so replays land on it."""
+def time_steps(group, singles, steps, warmup, stream, blocks=1):
+    """ms per step over `blocks` timed blocks of exactly `steps` steps each:
+    replays of `group` (one graph holding one step per rotating layer, back to
+    back as a model's layers are captured together), then single-step graphs
+    for the remainder.  CUDA events on `stream`, which is made current so
+    replays land on it; a barrier (synchronize) on both sides of each block.
+    Returns the per-block times (ms per step)."""
     per = len(singles)
+    out = []
     with torch.cuda.stream(stream):
-        for i in range(max(1, warmup // per)):
+        for i in range(max(1, -(-warmup // per))):
             group.replay()
         torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(steps // per):
-            group.replay()
-        for i in range(steps % per):
-            singles[i].replay()
-        t1.record(stream)
+        for _ in range(blocks):
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(steps // per):
+                group.replay()
+            for i in range(steps % per):
+                singles[i].replay()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            out.append(t0.elapsed_time(t1) / steps)
+    return out
+
+
+def spread(xs):
+    return {"median": round(statistics.median(xs), 5), "min": round(min(xs), 5),
+            "max": round(max(xs), 5), "blocks": len(xs)}
+
+
+def check_status(status, where):
     torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / steps
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x} in the {where} region")
+
+
+def e2e_leg(layers, step, stream, steps, warmup, world, depth=3):
+    """The step through the public API with host buffers: every step copies
+    its activations from pinned host memory, runs csa_decode and copies the
+    output back to pinned host memory, all inside the timed region.  Up to
+    `depth` steps are in flight (a serving loop's pipelining): step i waits
+    for the output of step i - depth before reusing its host buffer."""
+    hin = [(L.d.q_idx.cpu().pin_memory(), L.d.w_idx.cpu().pin_memory(),
+            L.d.q.cpu().pin_memory()) for L in layers]
+    hout = [torch.empty(layers[0].out.shape, dtype=torch.float32).pin_memory()
+            for _ in range(depth)]
+    done = [torch.cuda.Event() for _ in range(depth)]
+    n = max(3, steps)
+    with torch.cuda.stream(stream):
+        for i in range(warmup + n):
+            if i == warmup:
+                stream.synchronize()
+                t_start = time.perf_counter()
+            slot = i % depth
+            if i >= depth:
+                done[slot].synchronize()
+            L = layers[i % len(layers)]
+            hq_idx, hw_idx, hq = hin[i % len(layers)]
+            L.d.q_idx.copy_(hq_idx, non_blocking=True)
+            L.d.w_idx.copy_(hw_idx, non_blocking=True)
+            L.d.q.copy_(hq, non_blocking=True)
+            step(L, stream)
+            hout[slot].copy_(L.out, non_blocking=True)
+            done[slot].record(stream)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t_start) * 1e3 / n
+    hq_idx, hw_idx, hq = hin[0]
+    h2d = hq_idx.numel() * 2 + hw_idx.numel() * 4 + hq.numel() * 2
+    return {"value": round(world * 1e3 / e2e_ms, 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout[0].numel() * 4),
+            "ms_per_step": round(e2e_ms, 5), "in_flight": depth}
+
+
+def ctx64k_leg(device, csa, stream, status, reps, seed):
+    """The 64K workload's 100 consecutive decode steps: step i queries
+    position 65536 + i, appends that position's row to the window ring and,
+    when a block completes, makes it visible (its key and row are written into
+    the caches).  All 100 steps are captured in one graph (the ring is first
+    restored to step 0's contents) and replayed; value = steps / time."""
+    wl = W.ctx64k(seed=seed)
+    gen = torch.Generator().manual_seed(1234)
+    steps = 100
+    ring0 = wl.swa_kv.clone()
+    pos, off, first, rows, qi, wi, qq = [], [], [], [], [], [], []
+    for i in range(steps):
+        if i:
+            W.ctx64k_step(wl, i, gen)
+        p = int(wl.tok_pos[0])
+        pos.append(wl.tok_pos.clone())
+        off.append(wl.comp_off.clone())
+        first.append(wl.swa_first_pos.clone())
+        rows.append(wl.swa_kv[0, p % wl.swa_cap].clone())
+        qi.append(wl.q_idx.clone())
+        wi.append(wl.w_idx.clone())
+        qq.append(wl.q.clone())
+    d = wl.to(device)
+    d.swa_kv.copy_(ring0.to(device))
+    ring0_d = ring0.to(device)
+    pos_d = [x.to(device) for x in pos]
+    off_d = [x.to(device) for x in off]
+    first_d = [x.to(device) for x in first]
+    rows_d = torch.stack(rows).to(device)
+    qi_d = [x.to(device) for x in qi]
+    wi_d = [x.to(device) for x in wi]
+    qq_d = [x.to(device) for x in qq]
+    # cache rows written by the steps that complete a block (drawn with the buffers)
+    k_src = d.k_idx.clone()
+    kv_src = d.comp_kv.clone()
+    cap = int(wl.k_idx.shape[0])
+    prm = csa.params(wl.n_heads, wl.top_k, wl.window, wl.ratio, wl.scale)
+    lays = [csa.Layout(d.tok_seq, pos_d[i], off_d[i], d.swa_kv, first_d[i], max_comp_rows=cap,
+                       total_comp_rows=cap, swa_cap=wl.swa_cap) for i in range(steps)]
+    ws = csa.workspace(lays[0], prm)
+    out = torch.empty(1, wl.n_heads, wl.hd, dtype=torch.float32, device=device)
+
+    def run_all():
+        d.swa_kv.copy_(ring0_d)
+        for i in range(steps):
+            p = int(pos[i][0])
+            if i:
+                d.swa_kv[0, p % wl.swa_cap].copy_(rows_d[i])
+                if int(off[i][1]) > int(off[i - 1][1]):
+                    b = int(off[i][1]) - 1
+                    d.k_idx[b].copy_(k_src[b])
+                    d.comp_kv[b].copy_(kv_src[b])
+            csa.csa_decode(lays[i], prm, qi_d[i], wi_d[i], d.k_idx, d.comp_kv, qq_d[i], out,
+                           status, ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        run_all()
+    check_status(status, "64k")
+    g = capture(run_all, stream)
+    ms = time_graphs([g], reps, 2, stream)
+    check_status(status, "64k")
+    return {"workload": "64k: 100 consecutive decode steps at positions 65536..65635, "
+                        "16384..16408 visible blocks, top_k 1024, 64 heads; each step appends "
+                        "its window row, every 4th a compressed block; one graph of 100 steps",
+            "tokens_per_s_per_layer": round(steps * 1e3 / ms, 1),
+            "us_per_step": round(ms * 1e3 / steps, 3), "replays": reps,
+            "l2": "hot: one layer's 4 MiB of keys and 16 MiB of rows stay in L2 across steps"}
+
+
+def prefill_leg(args, device, csa, stream, status, rank, tf_peak, peak_kind):
+    """The indexer alone on a chunked-prefill workload: `args.prefill_tokens`
+    query tokens of one sequence at positions 262144.. share every key tile
+    (four tokens per MMA), timed from replays of a one-launch graph."""
+    pl = Layer(W.prefill(seed=900 + 1000 * rank, tokens=args.prefill_tokens, device=device),
+               device, csa)
+    pw = pl.wl
+    psc = torch.empty(pw.num_tokens, pw.max_comp_rows, dtype=torch.float32, device=device)
+
+    def pstep():
+        csa.csa_indexer_scores(pl.layout, pl.prm, pl.d.q_idx, pl.d.w_idx, pl.d.k_idx, psc,
+                               status, stream=stream)
+    with torch.cuda.stream(stream):
+        pstep()
+    torch.cuda.synchronize()
+    pgraph = capture(pstep, stream)
+    reps = max(3, min(20, args.steps // 10))
+    pms = time_graphs([pgraph], reps, 3, stream)
+    nvis = [min(int(pw.comp_off[1]), int(pw.tok_pos[t]) // pw.ratio)
+            for t in range(pw.num_tokens)]
+    flops = 2.0 * pw.n_ih * pw.ihd * float(sum(nvis))
+    tflops = flops / (pms * 1e-3) / 1e12
+    check_status(status, "prefill")
+    return {"workload": f"prefill: indexer alone, {pw.num_tokens} tokens at p = 262144.., "
+                        f"65,536..{max(nvis)} visible blocks each, 64 heads x 128",
+            "ms_per_launch": round(pms, 4), "tflops": round(tflops, 1),
+            "peak_tflops": tf_peak, "peak_kind": peak_kind + " bf16 burst",
+            "frac": round(tflops / tf_peak, 4), "launches": reps + 4}
 
 
 def run_ours(args, rank, world, device):
@@ -245,12 +399,12 @@ def run_ours(args, rank, world, device):
     hbm_peak, tf_peak, peak_kind = peaks()
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
 
     layers = make_layers("1m", args.layers, device, csa, seed0=1000 * rank)
     wl0 = layers[0].wl
     ab = algorithmic_bytes(wl0)
     ws = csa.workspace(layers[0].layout, layers[0].prm)
-    status = torch.zeros(1, dtype=torch.int32, device=device)
 
     def step(L, s):
         csa.csa_decode(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, L.d.comp_kv, L.d.q,
@@ -265,20 +419,22 @@ def run_ours(args, rank, world, device):
     group = capture(lambda: [step(L, stream) for L in layers], stream)
     per_step_launches = launches_in_graph(graphs[0])
 
-    # ---- timed region: exactly `steps` decode steps
+    # ---- timed region: `blocks` blocks of exactly `steps` decode steps
     if world > 1:
         torch.distributed.barrier()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
-    ms = time_steps(group, graphs, args.steps, args.warmup, stream)
+    blocks = time_steps(group, graphs, args.steps, args.warmup, stream, blocks=args.blocks)
     clk = clocks.stop()
-    ms = max_over_ranks(ms, device)
-    torch.cuda.synchronize()
-    st = int(status.item())
-    if st != 0:
-        raise RuntimeError(f"device status {st:#x} during the timed region")
+    ms = max_over_ranks(statistics.median(blocks), device)
+    check_status(status, "timed")
     assert torch.isfinite(layers[0].out).all()
+    # the step's own result for layer 0 (compared with the oracle in cpu_baseline)
+    with torch.cuda.stream(stream):
+        step(layers[0], stream)
+    torch.cuda.synchronize()
+    res0 = (layers[0].idx[0].cpu().numpy().copy(), layers[0].out[0].cpu().numpy().copy())
 
     # ---- the dominant kernel alone (indexer): one graph holds one launch per
     # rotating layer, so replays carry no host overhead; CUDA events on `stream`
@@ -293,37 +449,18 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     igraph = capture(index_all, stream)
     reps = max(1, args.steps // len(layers))
-    idx_ms = time_graphs([igraph], reps, max(1, args.warmup // len(layers)), stream) / len(layers)
+    idx_blocks = [time_graphs([igraph], reps, max(1, args.warmup // len(layers)), stream)
+                  / len(layers) for _ in range(args.blocks)]
+    idx_ms = statistics.median(idx_blocks)
 
+    line_extra = {}
     # ---- end to end through the public API with host buffers
-    e2e = None
     if not args.no_e2e:
-        L = layers[0]
-        hq_idx = L.d.q_idx.cpu().pin_memory()
-        hw_idx = L.d.w_idx.cpu().pin_memory()
-        hq = L.d.q.cpu().pin_memory()
-        hout = torch.empty(L.out.shape, dtype=torch.float32).pin_memory()
-        n_e2e = max(3, args.steps)
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup + n_e2e):
-                if i == args.warmup:
-                    torch.cuda.synchronize()
-                    t_start = time.perf_counter()
-                L = layers[i % len(layers)]
-                L.d.q_idx.copy_(hq_idx, non_blocking=True)
-                L.d.w_idx.copy_(hw_idx, non_blocking=True)
-                L.d.q.copy_(hq, non_blocking=True)
-                step(L, stream)
-                hout.copy_(L.out, non_blocking=True)
-                stream.synchronize()
-        e2e_ms = (time.perf_counter() - t_start) * 1e3 / n_e2e
-        h2d = hq_idx.numel() * 2 + hw_idx.numel() * 4 + hq.numel() * 2
-        e2e = {"value": round(world * 1e3 / e2e_ms, 1), "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 4)}
+        line_extra["e2e"] = e2e_leg(layers, step, stream, args.steps, args.warmup, world)
+        check_status(status, "e2e")
 
     # ---- next row: the same 1M step with the indexer keys cached as MXFP4
     # (80 bytes per key instead of 256); the cache is quantized once, untimed
-    fp4 = None
     if not args.no_fp4:
         frows = []
         for L in layers:
@@ -347,32 +484,37 @@ def run_ours(args, rank, world, device):
         torch.cuda.synchronize()
         fsingles = [capture(lambda i=i: fstep(i, stream), stream) for i in range(len(layers))]
         fgroup = capture(lambda: [fstep(i, stream) for i in range(len(layers))], stream)
-        fms = time_steps(fgroup, fsingles, args.steps, args.warmup, stream)
+        fms = statistics.median(time_steps(fgroup, fsingles, args.steps, args.warmup, stream,
+                                           blocks=args.blocks))
         figraph = capture(findex_all, stream)
         fims = time_graphs([figraph], max(1, args.steps // len(layers)),
                            max(1, args.warmup // len(layers)), stream) / len(layers)
         nv = ab["keys"] // (wl0.ihd * 2)
         fidx_bytes = nv * csa.FP4_ROW + (ab["indexer"] - ab["keys"])
         fstep_bytes = ab["step"] - ab["keys"] + nv * csa.FP4_ROW
-        fp4 = {"workload": "1m with MXFP4 indexer keys (80 B per key: 20 MiB instead of 64 MiB)",
-               "tokens_per_s_per_layer": round(world * 1e3 / fms, 1),
-               "ms_per_step": round(fms, 5), "indexer_ms": round(fims, 5),
-               "indexer_bytes_per_launch": int(fidx_bytes),
-               "indexer_hbm_frac": round(fidx_bytes / (fims * 1e-3) / 1e9 / hbm_peak, 4),
-               "step_algorithmic_bytes": int(fstep_bytes),
-               "step_hbm_frac": round(fstep_bytes / (fms * 1e-3) / 1e9 / hbm_peak, 4)}
+        line_extra["fp4"] = {
+            "workload": "1m with MXFP4 indexer keys (80 B per key: 20 MiB instead of 64 MiB)",
+            "tokens_per_s_per_layer": round(world * 1e3 / fms, 1),
+            "ms_per_step": round(fms, 5), "indexer_ms": round(fims, 5),
+            "indexer_bytes_per_launch": int(fidx_bytes),
+            "indexer_hbm_frac": round(fidx_bytes / (fims * 1e-3) / 1e9 / hbm_peak, 4),
+            "step_algorithmic_bytes": int(fstep_bytes),
+            "step_hbm_frac": round(fstep_bytes / (fms * 1e-3) / 1e9 / hbm_peak, 4)}
         del fsingles, fgroup, figraph, frows
-        torch.cuda.synchronize()
-        if int(status.item()) != 0:
-            raise RuntimeError("device status set in the FP4 region")
+        check_status(status, "FP4")
+
+    del graphs, group
+    # ---- the 64K workload: 100 consecutive decode steps of one layer
+    if not args.no_64k:
+        torch.cuda.empty_cache()
+        line_extra["ctx64k"] = ctx64k_leg(device, csa, stream, status,
+                                          reps=max(3, args.steps // 10), seed=7 + 1000 * rank)
 
     # ---- secondary: batched decode, 32 ragged sequences (32K..128K)
-    batch = None
     if not args.no_batch32:
-        del graphs
+        torch.cuda.empty_cache()
         blayers = make_layers("batch32", 2, device, csa, seed0=77 + 1000 * rank)
         bws = csa.workspace(blayers[0].layout, blayers[0].prm)
-        bgraphs = []
 
         def bstep(L, s):
             csa.csa_decode(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, L.d.comp_kv, L.d.q,
@@ -383,19 +525,21 @@ def run_ours(args, rank, world, device):
         torch.cuda.synchronize()
         bgraphs = [capture(lambda L=L: bstep(L, stream), stream) for L in blayers]
         bgroup = capture(lambda: [bstep(L, stream) for L in blayers], stream)
-        bms = time_steps(bgroup, bgraphs, args.steps, args.warmup, stream)
+        bms = statistics.median(time_steps(bgroup, bgraphs, args.steps, args.warmup, stream,
+                                           blocks=args.blocks))
         bab = sum(algorithmic_bytes(L.wl)["step"] for L in blayers) / len(blayers)
-        batch = {"workload": "batch32: 32 sequences, contexts U{32K..128K}, one token each",
-                 "tokens_per_s_per_layer": round(32 * 1e3 / bms, 1), "ms_per_step": round(bms, 5),
-                 "algorithmic_bytes_per_step": int(bab),
-                 "hbm_frac": round(bab / (bms * 1e-3) / 1e9 / hbm_peak, 4)}
-        torch.cuda.synchronize()
-        if int(status.item()) != 0:
-            raise RuntimeError("device status set in the batch32 region")
+        line_extra["batch32"] = {
+            "workload": "batch32: 32 sequences, contexts U{32K..128K}, one token each",
+            "tokens_per_s_per_layer": round(32 * 1e3 / bms, 1), "ms_per_step": round(bms, 5),
+            "algorithmic_bytes_per_step": int(bab),
+            "hbm_frac": round(bab / (bms * 1e-3) / 1e9 / hbm_peak, 4),
+            "launches_per_step": launches_in_graph(bgraphs[0])}
+        del bgraphs, bgroup, blayers
+        check_status(status, "batch32")
 
     # ---- next row: HCA decode at 1M context (8192 compressed rows, dense)
-    hca = None
     if not args.no_hca:
+        torch.cuda.empty_cache()
         hl = [W.hca1m(seed=500 + i + 1000 * rank, device=device) for i in range(32)]
         hd = []
         for wl in hl:
@@ -416,59 +560,33 @@ def run_ours(args, rank, world, device):
         torch.cuda.synchronize()
         hgraphs = [capture(lambda x=x: hstep(x, stream), stream) for x in hd]
         hgroup = capture(lambda: [hstep(x, stream) for x in hd], stream)
-        hms = time_steps(hgroup, hgraphs, args.steps, args.warmup, stream)
-        hab = algorithmic_bytes(hl[0])
+        hms = statistics.median(time_steps(hgroup, hgraphs, args.steps, args.warmup, stream,
+                                           blocks=args.blocks))
         hbytes = (8192 + 128) * 1024 + 64 * 1024 + 64 * 2048
-        hca = {"workload": "hca1m: HCA decode, 1 token, ratio 128, 8192 compressed rows + 128 "
-                           "window rows, 64 heads, dense (32 rotating layers, 270 MB)",
-               "tokens_per_s_per_layer": round(world * 1e3 / hms, 1),
-               "ms_per_step": round(hms, 5), "algorithmic_bytes_per_step": hbytes,
-               "hbm_frac": round(hbytes / (hms * 1e-3) / 1e9 / hbm_peak, 4),
-               "launches_per_step": launches_in_graph(hgraphs[0])}
-        del hab
-        torch.cuda.synchronize()
-        if int(status.item()) != 0:
-            raise RuntimeError("device status set in the HCA region")
+        line_extra["hca"] = {
+            "workload": "hca1m: HCA decode, 1 token, ratio 128, 8192 compressed rows + 128 "
+                        "window rows, 64 heads, dense (32 rotating layers, 270 MB)",
+            "tokens_per_s_per_layer": round(world * 1e3 / hms, 1),
+            "ms_per_step": round(hms, 5), "algorithmic_bytes_per_step": hbytes,
+            "hbm_frac": round(hbytes / (hms * 1e-3) / 1e9 / hbm_peak, 4),
+            "launches_per_step": launches_in_graph(hgraphs[0])}
+        del hd, hgraphs, hgroup, hl
+        check_status(status, "HCA")
 
-    # ---- prefill indexer alone: 4096 query tokens of one sequence share every
-    # key tile (four tokens per MMA), the tensor-bound case
-    prefill = None
+    # ---- prefill indexer alone: query tokens of one sequence share every key
+    # tile (four tokens per MMA), the tensor-bound case
     if not args.no_prefill:
-        if "hd" in locals():
-            del hd, hgraphs, hgroup
         torch.cuda.empty_cache()
-        pl = Layer(W.prefill(seed=900 + 1000 * rank, device=device), device, csa)
-        pw = pl.wl
-        psc = torch.empty(pw.num_tokens, pw.max_comp_rows, dtype=torch.float32, device=device)
-
-        def pstep():
-            csa.csa_indexer_scores(pl.layout, pl.prm, pl.d.q_idx, pl.d.w_idx, pl.d.k_idx, psc,
-                                   status, stream=stream)
-        with torch.cuda.stream(stream):
-            pstep()
-        torch.cuda.synchronize()
-        pgraph = capture(pstep, stream)
-        reps = max(3, min(20, args.steps // 10))
-        pms = time_graphs([pgraph], reps, 3, stream)
-        nvis = [min(int(pw.comp_off[1]), int(pw.tok_pos[t]) // pw.ratio)
-                for t in range(pw.num_tokens)]
-        flops = 2.0 * pw.n_ih * pw.ihd * float(sum(nvis))
-        tflops = flops / (pms * 1e-3) / 1e12
-        prefill = {"workload": "prefill: indexer alone, 4096 tokens at p = 262144.., "
-                               "65,536..66,559 visible blocks each, 64 heads x 128",
-                   "ms_per_launch": round(pms, 4), "tflops": round(tflops, 1),
-                   "peak_tflops": tf_peak, "peak_kind": peak_kind + " bf16 burst",
-                   "frac": round(tflops / tf_peak, 4), "launches": reps}
-        del psc, pl
-        torch.cuda.synchronize()
-        if int(status.item()) != 0:
-            raise RuntimeError("device status set in the prefill region")
+        line_extra["prefill_indexer"] = prefill_leg(args, device, csa, stream, status, rank,
+                                                    tf_peak, peak_kind)
 
     tok_s = world * 1e3 / ms
     achieved = ab["indexer"] / (idx_ms * 1e-3) / 1e9
+    n_vis0 = ab["keys"] // (wl0.ihd * 2)
     line = {
         "metric": METRIC, "value": round(tok_s, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "ms_per_step_blocks": spread(blocks),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "1m: CSA decode, 1 token, 262144 blocks (64 MiB keys, 256 MiB "
@@ -482,21 +600,19 @@ def run_ours(args, rank, world, device):
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": indexer_traffic(),
                      "peak_kind": peak_kind, "kernel_ms": round(idx_ms, 5),
+                     "kernel_ms_blocks": spread(idx_blocks),
                      "bytes_per_launch": ab["indexer"]},
+        "indexer_keys_per_s": round(n_vis0 / (idx_ms * 1e-3), 1),
         "step_roofline": {"bound": "hbm", "algorithmic_bytes": ab["step"],
                           "achieved": round(ab["step"] / (ms * 1e-3) / 1e9, 1),
                           "peak": hbm_peak, "unit": "GB/s",
                           "frac": round(ab["step"] / (ms * 1e-3) / 1e9 / hbm_peak, 4)},
         "gpu_launches": per_step_launches * args.steps if per_step_launches > 0 else None,
         "launches_per_step": per_step_launches,
-        "e2e": e2e,
         "clocks": clk,
-        "batch32": batch,
-        "hca": hca,
-        "prefill_indexer": prefill,
-        "fp4": fp4,
     }
-    return line
+    line.update(line_extra)
+    return line, wl0, res0
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -509,19 +625,35 @@ def oracle_step(wl):
                          window=wl.window, ratio=wl.ratio, scale=wl.scale)
 
 
-def cpu_baseline(steps: int):
-    """The oracle as it stands, on full 1M decode steps (one token, one layer each)."""
+def cpu_baseline(steps: int, wl=None, gpu=None):
+    """The oracle as it stands, on full 1M decode steps (one token, one layer
+    each), on the GPU leg's first layer when given (else a fresh seeded one).
+    With the GPU's result for that layer, also its recall against the
+    oracle's selection and the max-abs difference of the outputs."""
     import oracle
     oracle.build()
-    wl = W.ctx1m(seed=0)
-    oracle_step(wl)   # warm (page in)
+    wl = W.ctx1m(seed=0) if wl is None else wl.to("cpu")
+    idx, n_sel, out = oracle_step(wl)   # warm (page in) and the reference result
     t0 = time.perf_counter()
     for _ in range(steps):
         oracle_step(wl)
     dt = (time.perf_counter() - t0) / steps
-    return {"value": round(1.0 / dt, 4), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{steps} full 1m decode steps (262144 blocks, top_k 1024, 64 heads), f64"}
+    res = {"value": round(1.0 / dt, 4), "unit": UNIT, "cores": oracle.num_threads(),
+           "kind": "oracle",
+           "sample": f"{steps} full 1m decode steps (262144 blocks, top_k 1024, 64 heads), f64"}
+    if gpu is not None:
+        gidx, gout = gpu
+        k = int(n_sel[0])
+        ref = set(idx[0, :k].tolist())
+        got = set(int(x) for x in gidx if x >= 0)
+        res["vs_gpu"] = {
+            "recall": round(len(ref & got) / max(1, len(ref)), 6),
+            "max_abs_err": float(np.abs(gout.astype(np.float64) - out[0]).max()),
+            "planted_selected": int(len(set(wl.planted.tolist()) & got))
+            if wl.planted is not None else None,
+            "what": "GPU csa_decode on the timed layer 0 vs the f64 oracle's whole step "
+                    "(its own selection)"}
+    return res
 
 
 class OracleSlices:
@@ -608,6 +740,12 @@ def main():
     ap.add_argument("--no-hca", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-fp4", action="store_true")
+    ap.add_argument("--no-64k", action="store_true")
+    ap.add_argument("--blocks", type=int, default=5,
+                    help="timed blocks of --steps steps each; the median is reported")
+    ap.add_argument("--prefill-tokens", type=int, default=4096)
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prefill-indexer leg and print its object (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -625,9 +763,20 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     device = torch.device("cuda", local)
-    line = run_ours(args, rank, world, device)
+    if args.prefill_only:
+        from sparse_compressed_kv_gb300 import build as cuda_build
+        from sparse_compressed_kv_gb300 import csa
+        cuda_build.build()
+        _, tf_peak, peak_kind = peaks()
+        torch.cuda.set_device(device)
+        stream = torch.cuda.Stream(device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        print(json.dumps(prefill_leg(args, device, csa, stream, status, rank, tf_peak,
+                                     peak_kind)), flush=True)
+        return
+    line, wl0, res0 = run_ours(args, rank, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_steps)
+        line["cpu_baseline"] = cpu_baseline(args.cpu_steps, wl0, res0)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

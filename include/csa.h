@@ -252,10 +252,12 @@ csa_status_t csa_decode_fp4(const csa_layout_t *layout, const csa_params_t *para
  * csa_topk the workspace it needs.  The pages have no counterpart: this is a
  * deployment convenience, not a step of the method.
  *
- * Same arguments, results and errors as csa_topk minus ws/ws_bytes.  The
+ * Same arguments, results and errors as csa_topk minus ws/ws_bytes (the
+ * same checks run in the same order, so a bad input gets the same code).  The
  * scratch is a fixed 260 KiB array inside libcsa.so, reserved on every GPU
  * that loads the library until the process exits; it limits a call to at
- * most 16 query tokens (more returns CSA_ERR_CAPACITY) and top_k <= 2048.
+ * most 16 query tokens: more returns CSA_ERR_CAPACITY.  top_k above 2048
+ * returns CSA_ERR_UNSUPPORTED, as it does for csa_topk.
  * Each token's selection runs in one thread block here, so long rows take
  * longer than with csa_topk.
  * The first call on a device looks up the array's device address (a one-time

@@ -116,7 +116,7 @@ static int g_dev_ok[64];          // 0 unknown, 1 ok, -1 unsupported
 static int g_dev_sms[64];
 static std::mutex g_dev_mu;
 
-static csa_status_t current_device(int *sms) {
+csa_status_t current_device(int *sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
     if (dev < 0 || dev >= 64) return CSA_ERR_UNSUPPORTED;
@@ -136,15 +136,11 @@ static csa_status_t current_device(int *sms) {
     return CSA_OK;
 }
 
-}  // namespace csa
-
-using namespace csa;
-
 // ---------------------------------------------------------------- validation
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static csa_status_t check_params(const csa_params_t *p) {
+csa_status_t check_params(const csa_params_t *p) {
     if (!p) return CSA_ERR_INVALID_ARGUMENT;
     if (p->n_ih != kNIH || p->ihd != kIHD || p->hd != kHD) return CSA_ERR_UNSUPPORTED;
     if (p->n_heads < kHeadGroup || p->n_heads > 128 || p->n_heads % kHeadGroup) return CSA_ERR_UNSUPPORTED;
@@ -155,7 +151,7 @@ static csa_status_t check_params(const csa_params_t *p) {
     return CSA_OK;
 }
 
-static csa_status_t check_layout(const csa_layout_t *L, const csa_params_t *p, bool need_swa) {
+csa_status_t check_layout(const csa_layout_t *L, const csa_params_t *p, bool need_swa) {
     if (!L) return CSA_ERR_INVALID_ARGUMENT;
     if (L->num_seqs < 1 || L->num_tokens < 0) return CSA_ERR_INVALID_ARGUMENT;
     if (L->total_comp_rows < 0 || L->max_comp_rows < 0) return CSA_ERR_INVALID_ARGUMENT;
@@ -174,6 +170,10 @@ static csa_status_t check_layout(const csa_layout_t *L, const csa_params_t *p, b
     }
     return CSA_OK;
 }
+
+}  // namespace csa
+
+using namespace csa;
 
 static csa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 

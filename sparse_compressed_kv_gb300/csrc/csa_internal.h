@@ -42,6 +42,13 @@ struct WsPlan {
     size_t total = 0;        // state + data + alignment slack
 };
 
+// Host-side argument checks shared by the entry points (csa_api.cu).  Each
+// returns CSA_OK or the csa_status_t the entry point reports.
+csa_status_t check_params(const csa_params_t *p);
+csa_status_t check_layout(const csa_layout_t *L, const csa_params_t *p, bool need_swa);
+// The current device is an sm_103 part; *sms = its SM count (cached per device).
+csa_status_t current_device(int *sms);
+
 // rows_max: most rows any token attends (top_k + window for CSA; for HCA,
 // every visible block + window); < 0 means top_k + window.
 WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_t rows_max = -1);

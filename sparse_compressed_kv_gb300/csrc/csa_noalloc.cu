@@ -46,27 +46,22 @@ using namespace csa;
 extern "C" csa_status_t csa_topk_noalloc(const csa_layout_t *layout, const csa_params_t *params,
                                          const float *scores, int64_t ld_scores, int32_t *idx,
                                          int32_t *n_sel, int32_t *dev_status, void *stream) {
-    if (!layout || !params) return CSA_ERR_INVALID_ARGUMENT;
-    if (params->n_ih != kNIH || params->ihd != kIHD || params->hd != kHD) return CSA_ERR_UNSUPPORTED;
-    if (params->top_k < 1 || params->ratio < 1) return CSA_ERR_INVALID_ARGUMENT;
-    if (params->top_k > kMaxTopK) return CSA_ERR_UNSUPPORTED;
-    if (layout->num_seqs < 1 || layout->num_tokens < 0 || layout->max_comp_rows < 0 ||
-        layout->total_comp_rows < layout->max_comp_rows)
-        return CSA_ERR_INVALID_ARGUMENT;
+    // the same checks, in the same order, as csa_topk; only the token limit
+    // of the fixed scratch is this entry point's own
+    csa_status_t st = check_params(params);
+    if (st != CSA_OK) return st;
+    st = check_layout(layout, params, false);
+    if (st != CSA_OK) return st;
     if (layout->num_tokens == 0) return CSA_OK;
-    // beyond the static scratch: refuse instead of overrunning it
-    if (layout->num_tokens > kNoAllocMaxTokens) return CSA_ERR_CAPACITY;
-    if (!layout->tok_seq || !layout->tok_pos || !layout->comp_off) return CSA_ERR_INVALID_ARGUMENT;
     if (!scores || !idx || !n_sel || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
     if (ld_scores < layout->max_comp_rows || ld_scores < 1) return CSA_ERR_CAPACITY;
+    // beyond the static scratch: refuse instead of overrunning it
+    if (layout->num_tokens > kNoAllocMaxTokens) return CSA_ERR_CAPACITY;
 
-    int dev = 0, sms = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return CSA_ERR_CUDA;
-    if (major != 10 || minor != 3) return CSA_ERR_UNSUPPORTED;
+    int sms = 0, dev = 0;
+    st = current_device(&sms);
+    if (st != CSA_OK) return st;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
     void *base = nullptr;
     if (scratch_address(dev, &base) != cudaSuccess) return CSA_ERR_CUDA;
 

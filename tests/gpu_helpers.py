@@ -23,6 +23,33 @@ def bits_to_f64(b):
     return (np.asarray(b).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+# Canary guard bands: every buffer a library call writes is allocated with
+# GUARD bytes of a known pattern on each side, checked after the call.  A
+# write just past (or before) an output, the workspace included, fails the
+# test even when the values inside the buffer are right.
+GUARD = 4096
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """A device tensor of `shape` with guard bands on both sides (offsets keep
+    the 256-byte alignment of the allocation)."""
+
+    def __init__(self, shape, dtype, device, fill=None):
+        elem = torch.empty((), dtype=dtype).element_size()
+        n = int(np.prod(shape))
+        g = GUARD // elem
+        self.raw = torch.empty(n + 2 * g, dtype=dtype, device=device)
+        self.raw.view(torch.uint8).fill_(GUARD_BYTE)
+        self.t = self.raw[g:g + n].view(*shape)
+        if fill is not None:
+            self.t.fill_(fill)
+
+    def intact(self) -> bool:
+        b = self.raw.view(torch.uint8)
+        return bool((b[:GUARD] == GUARD_BYTE).all()) and bool((b[-GUARD:] == GUARD_BYTE).all())
+
+
 class Run:
     """One workload on the GPU, with its layout, params and workspace."""
 
@@ -36,10 +63,23 @@ class Run:
                                  max_comp_rows=mcr,
                                  total_comp_rows=int(wl.k_idx.shape[0]), swa_cap=wl.swa_cap)
         self.prm = csa.params(wl.n_heads, wl.top_k, wl.window, wl.ratio, wl.scale)
-        self.ws = csa.workspace(self.layout, self.prm)
+        self.guards = []
+        self.ws = self.buf((csa.csa_workspace_size(self.layout, self.prm),), torch.uint8, 0)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.T = wl.num_tokens
         self.ld = mcr
+
+    def buf(self, shape, dtype, fill):
+        g = Guarded(shape, dtype, self.dev, fill)
+        self.guards.append(g)
+        return g.t
+
+    def check_guards(self):
+        torch.cuda.synchronize()
+        bad = [i for i, g in enumerate(self.guards) if not g.intact()]
+        assert not bad, f"guard band overwritten around buffer(s) {bad}"
+        # forget output buffers (keep the workspace): memory stays bounded
+        self.guards = self.guards[:1]
 
     # -- oracle-side views
     def n_vis(self):
@@ -50,41 +90,44 @@ class Run:
             out.append(oracle.n_vis(n_comp, int(self.wl.tok_pos[t]), self.wl.ratio))
         return out
 
-    # -- GPU calls
+    # -- GPU calls (each checks the guard bands of what it wrote)
     def scores(self):
-        sc = torch.full((self.T, self.ld), float("nan"), dtype=torch.float32, device=self.dev)
+        sc = self.buf((self.T, self.ld), torch.float32, float("nan"))
         csa.csa_indexer_scores(self.layout, self.prm, self.d.q_idx, self.d.w_idx, self.d.k_idx,
                                sc, self.status)
+        self.check_guards()
         return sc
 
     def topk(self, scores):
-        idx = torch.full((self.T, self.wl.top_k), -7, dtype=torch.int32, device=self.dev)
-        n_sel = torch.full((self.T,), -7, dtype=torch.int32, device=self.dev)
+        idx = self.buf((self.T, self.wl.top_k), torch.int32, -7)
+        n_sel = self.buf((self.T,), torch.int32, -7)
         csa.csa_topk(self.layout, self.prm, scores, idx, n_sel, self.status, self.ws)
+        self.check_guards()
         return idx, n_sel
 
     def gather(self, idx, n_sel):
         rows = self.wl.top_k + self.wl.window
-        kv_buf = torch.zeros((self.T, rows, self.wl.hd), dtype=torch.bfloat16, device=self.dev)
-        kv_len = torch.full((self.T,), -7, dtype=torch.int32, device=self.dev)
+        kv_buf = self.buf((self.T, rows, self.wl.hd), torch.bfloat16, 0)
+        kv_len = self.buf((self.T,), torch.int32, -7)
         csa.csa_gather_mixed(self.layout, self.prm, idx, n_sel, self.d.comp_kv, kv_buf, kv_len,
                              self.status)
+        self.check_guards()
         return kv_buf, kv_len
 
     def attention(self, kv_buf, kv_len, sinks=None):
-        out = torch.full((self.T, self.wl.n_heads, self.wl.hd), float("nan"), dtype=torch.float32,
-                         device=self.dev)
+        out = self.buf((self.T, self.wl.n_heads, self.wl.hd), torch.float32, float("nan"))
         csa.csa_sparse_mqa_decode(self.prm, self.d.q, kv_buf, kv_len, out, self.status, self.ws,
                                   sinks=sinks)
+        self.check_guards()
         return out
 
     def decode(self, sinks=None):
-        out = torch.full((self.T, self.wl.n_heads, self.wl.hd), float("nan"), dtype=torch.float32,
-                         device=self.dev)
-        idx = torch.full((self.T, self.wl.top_k), -7, dtype=torch.int32, device=self.dev)
+        out = self.buf((self.T, self.wl.n_heads, self.wl.hd), torch.float32, float("nan"))
+        idx = self.buf((self.T, self.wl.top_k), torch.int32, -7)
         csa.csa_decode(self.layout, self.prm, self.d.q_idx, self.d.w_idx, self.d.k_idx,
                        self.d.comp_kv, self.d.q, out, self.status, self.ws, idx_out=idx,
                        sinks=sinks)
+        self.check_guards()
         return out, idx
 
     def dev_status(self):

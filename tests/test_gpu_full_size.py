@@ -113,6 +113,14 @@ def test_64k_decode_loop(cuda_device):
             run.d.w_idx.copy_(wl.w_idx)
             run.d.q.copy_(wl.q)
         out, fidx = run.decode()
+        if i == 1:
+            # after one full round of calls every buffer size has been seen:
+            # from here on nothing may allocate device memory ("1M-context
+            # viability", falsifiable gate A4: memory_reserved flat across
+            # decode steps); the library itself never allocates at all
+            torch.cuda.synchronize()
+            reserved0 = torch.cuda.memory_reserved()
+            free0 = torch.cuda.mem_get_info()[0]
         if i % 9 == 0 or i == 99:
             sc = run.scores()
             idx, n_sel = run.topk(sc)
@@ -121,3 +129,8 @@ def test_64k_decode_loop(cuda_device):
             kv_buf, kv_len = H.gpu_rows(run, idx, n_sel)
             H.check_attention(wl, kv_buf, kv_len, out)
     assert run.dev_status() == 0
+    # the pages' gate: reserved memory flat within 50 MB over the loop; and the
+    # device's free memory moved by no more than what torch itself reserved
+    grown = torch.cuda.memory_reserved() - reserved0
+    assert abs(grown) <= 50 << 20
+    assert abs((free0 - torch.cuda.mem_get_info()[0]) - grown) <= 2 << 20

@@ -99,3 +99,59 @@ def test_binding_refuses_host_tensors(lib):
     import torch
     with pytest.raises(ValueError):
         csa._p(torch.zeros(4))
+
+
+def _noalloc(lib):
+    fn = lib.csa_topk_noalloc
+    fn.argtypes = [ctypes.POINTER(csa.csa_layout_t), ctypes.POINTER(csa.csa_params_t),
+                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+@pytest.mark.parametrize("case", ["n_heads", "scale", "top_k0", "top_k2049", "rows2g",
+                                  "no_tok_seq", "ld", "maxr", "null_idx"])
+def test_noalloc_rejects_what_topk_rejects(lib, case):
+    """csa_topk_noalloc returns the code csa_topk returns for the same bad
+    input (both decide before any device call)."""
+    dummy = ctypes.c_void_p(256)
+    P = csa.params(16, 64)
+    L = _layout(R=1000, maxr=1000)
+    L.tok_seq = L.tok_pos = L.comp_off = dummy
+    ld = 1000
+    idx = dummy
+    if case == "n_heads":
+        P.n_heads = 24
+    elif case == "scale":
+        P.scale = float("nan")
+    elif case == "top_k0":
+        P.top_k = 0
+    elif case == "top_k2049":
+        P.top_k = 2049
+    elif case == "rows2g":
+        L = _layout(R=1 << 31, maxr=1000)
+        L.tok_seq = L.tok_pos = L.comp_off = dummy
+    elif case == "no_tok_seq":
+        L.tok_seq = None
+    elif case == "ld":
+        ld = 999
+    elif case == "maxr":
+        L = _layout(R=10, maxr=20)
+        L.tok_seq = L.tok_pos = L.comp_off = dummy
+    elif case == "null_idx":
+        idx = None
+    want = lib.csa_topk(ctypes.byref(L), ctypes.byref(P), dummy, ld, idx, dummy, dummy, None, 0,
+                        None)
+    got = _noalloc(lib)(ctypes.byref(L), ctypes.byref(P), dummy, ld, idx, dummy, dummy, None)
+    assert want != 0 and want != 7      # decided before the workspace check
+    assert got == want
+
+
+def test_noalloc_token_limit_is_a_capacity_error(lib):
+    dummy = ctypes.c_void_p(256)
+    P = csa.params(16, 64)
+    L = _layout(T=17, R=1000, maxr=1000)
+    L.tok_seq = L.tok_pos = L.comp_off = dummy
+    assert _noalloc(lib)(ctypes.byref(L), ctypes.byref(P), dummy, 1000, dummy, dummy, dummy,
+                         None) == 3

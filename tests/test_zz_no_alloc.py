@@ -45,8 +45,15 @@ def _noalloc_topk(run, scores, idx, n_sel):
 ], ids=["two-sequences", "three-tokens"])
 def test_noalloc_topk_matches_workspace_topk_twice(cuda_device, wl_fn):
     run = H.Run(wl_fn(), cuda_device)
-    scores = run.scores()
+    _check_twice(run, run.scores())
+
+
+def _check_twice(run, scores):
+    """Two calls in a row: each equal to csa_topk with a workspace, bit for
+    bit, and to the oracle's selection on the same scores."""
     ref_idx, ref_n = run.topk(scores)
+    torch.cuda.synchronize()
+    H.check_topk_exact(run.wl, scores, ref_idx, ref_n)
     for _ in range(2):
         idx = torch.full_like(ref_idx, -9)
         n_sel = torch.full_like(ref_n, -9)
@@ -54,7 +61,28 @@ def test_noalloc_topk_matches_workspace_topk_twice(cuda_device, wl_fn):
         torch.cuda.synchronize()
         assert torch.equal(idx, ref_idx)
         assert torch.equal(n_sel, ref_n)
+        H.check_topk_exact(run.wl, scores, idx, n_sel)
     assert run.dev_status() == 0
+
+
+def test_noalloc_topk_sixteen_tokens(cuda_device):
+    # the largest call the fixed scratch takes: every token's state in use
+    run = H.Run(W.make("noalloc-16", seed=44, seq_lens=[4 * 3000], tokens=[16], top_k=512,
+                       n_heads=16), cuda_device)
+    _check_twice(run, run.scores())
+
+
+def test_noalloc_topk_all_equal_row(cuda_device):
+    # w = 0: every score is 0, so every entry shares the threshold digit and
+    # the per-warp staging overflows; the one-block path then re-reads the row
+    wl = W.make("noalloc-flat", seed=45, seq_lens=[4 * 20000, 4 * 700], tokens=[1, 1],
+                n_comp=[20000, 700], top_k=1000, n_heads=16)
+    wl.w_idx[0].zero_()
+    run = H.Run(wl, cuda_device)
+    scores = run.scores()
+    torch.cuda.synchronize()
+    assert (scores.cpu()[0, :20000] == 0).all()
+    _check_twice(run, scores)
 
 
 def test_noalloc_topk_rejects_too_many_tokens(cuda_device):
@@ -64,3 +92,15 @@ def test_noalloc_topk_rejects_too_many_tokens(cuda_device):
     idx = torch.empty(17, 64, dtype=torch.int32, device=cuda_device)
     n_sel = torch.empty(17, dtype=torch.int32, device=cuda_device)
     assert _noalloc_topk(run, scores, idx, n_sel) == 3   # CSA_ERR_CAPACITY
+
+
+def test_noalloc_topk_rejects_top_k_above_2048(cuda_device):
+    # the same code as csa_topk: the selection size is unsupported, not a
+    # capacity limit of the fixed scratch
+    run = H.Run(W.make("noalloc-d", seed=46, seq_lens=[4 * 3000], tokens=[1], top_k=64,
+                       n_heads=16), cuda_device)
+    scores = run.scores()
+    run.prm.top_k = 2049
+    idx = torch.empty(1, 2049, dtype=torch.int32, device=cuda_device)
+    n_sel = torch.empty(1, dtype=torch.int32, device=cuda_device)
+    assert _noalloc_topk(run, scores, idx, n_sel) == 2   # CSA_ERR_UNSUPPORTED
