@@ -112,8 +112,9 @@ const char *csa_status_string(csa_status_t status);
 /* CSA_ABI_VERSION of the loaded library. */
 int32_t csa_abi_version(void);
 
-/* Bytes of workspace `ws` that csa_topk, csa_sparse_mqa_decode and csa_decode
- * need for this layout and these params (one size serves all three).
+/* Bytes of workspace `ws` that csa_topk, csa_indexer_topk,
+ * csa_sparse_mqa_decode and csa_decode need for this layout and these params
+ * (one size serves all of them).
  * The workspace is device memory, 256-byte aligned, owned by the caller.
  * Its front holds per-token top-k state (16640 bytes per token) that must be
  * zero when a call starts: zero-fill the workspace once after allocating it.
@@ -151,6 +152,23 @@ csa_status_t csa_indexer_scores(const csa_layout_t *layout, const csa_params_t *
 csa_status_t csa_topk(const csa_layout_t *layout, const csa_params_t *params,
                       const float *scores, int64_t ld_scores, int32_t *idx, int32_t *n_sel,
                       int32_t *dev_status, void *ws, size_t ws_bytes, void *stream);
+
+/* Steps 1 and 2 in one call ([Audit rewrite], F3: the scores feed
+ * total.topk): idx / n_sel exactly as csa_topk writes them for the scores
+ * csa_indexer_scores computes, without handing the scores to the caller.
+ * For decode batches (one query token per key tile: more than one sequence,
+ * or fewer than four tokens) the selection runs inside the indexer kernel:
+ * each CTA keeps the candidates of its key range on chip and the last one to
+ * finish a token selects from them (an exact fallback over the token's whole
+ * score row covers the inputs where the candidates cannot prove the result,
+ * such as long runs of tied scores).  Other layouts run the indexer and
+ * csa_topk's kernels back to back.
+ *   q_idx bf16 [T, n_ih, ihd], w_idx f32 [T, n_ih], k_idx bf16 [R, ihd],
+ *   idx int32 [T, top_k], n_sel int32 [T], ws as for csa_topk. */
+csa_status_t csa_indexer_topk(const csa_layout_t *layout, const csa_params_t *params,
+                              const void *q_idx, const float *w_idx, const void *k_idx,
+                              int32_t *idx, int32_t *n_sel, int32_t *dev_status, void *ws,
+                              size_t ws_bytes, void *stream);
 
 /* Step 3, mixed gather into a caller-owned buffer ([Audit 1M], D3 and D5;
  * [Audit rewrite], C2):

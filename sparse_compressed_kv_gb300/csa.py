@@ -26,7 +26,7 @@ DEV_BAD_INDEX, DEV_MISSING_SWA, DEV_BAD_LAYOUT = 0x01, 0x02, 0x04
 DEV_CAPACITY, DEV_BAD_LENGTH, DEV_TIMEOUT = 0x08, 0x10, 0x20
 
 EXPORTS = ("csa_status_string", "csa_abi_version", "csa_workspace_size", "csa_indexer_scores",
-           "csa_topk", "csa_gather_mixed", "csa_sparse_mqa_decode", "csa_decode",
+           "csa_topk", "csa_indexer_topk", "csa_gather_mixed", "csa_sparse_mqa_decode", "csa_decode",
            "csa_hca_workspace_size", "csa_hca_decode", "csa_fp4_quantize_keys",
            "csa_indexer_scores_fp4", "csa_decode_fp4")
 FP4_ROW = 80  # bytes per MXFP4 key row (include/csa.h)
@@ -78,6 +78,7 @@ def load() -> ctypes.CDLL:
     lib.csa_workspace_size.argtypes = [L, Pm, ctypes.POINTER(sz)]
     lib.csa_indexer_scores.argtypes = [L, Pm, P, P, P, P, i64, P, P]
     lib.csa_topk.argtypes = [L, Pm, P, i64, P, P, P, P, sz, P]
+    lib.csa_indexer_topk.argtypes = [L, Pm, P, P, P, P, P, P, P, sz, P]
     lib.csa_gather_mixed.argtypes = [L, Pm, P, P, P, P, P, P, P]
     lib.csa_sparse_mqa_decode.argtypes = [i32, Pm, P, P, P, P, P, P, P, sz, P]
     lib.csa_decode.argtypes = [L, Pm, P, P, P, P, P, P, P, P, P, P, sz, P]
@@ -178,6 +179,14 @@ def csa_topk(layout: Layout, prm: csa_params_t, scores, idx, n_sel, dev_status, 
     _check("csa_topk", load().csa_topk(
         ctypes.byref(lc), ctypes.byref(prm), _p(scores), int(scores.shape[1]), _p(idx),
         _p(n_sel), _p(dev_status), _p(ws), int(ws.numel()), _stream(stream)))
+
+
+def csa_indexer_topk(layout: Layout, prm: csa_params_t, q_idx, w_idx, k_idx, idx, n_sel,
+                     dev_status, ws, stream=None):
+    lc = layout.c()
+    _check("csa_indexer_topk", load().csa_indexer_topk(
+        ctypes.byref(lc), ctypes.byref(prm), _p(q_idx), _p(w_idx), _p(k_idx), _p(idx), _p(n_sel),
+        _p(dev_status), _p(ws), int(ws.numel()), _stream(stream)))
 
 
 def csa_gather_mixed(layout: Layout, prm: csa_params_t, idx, n_sel, comp_kv, kv_buf, kv_len,

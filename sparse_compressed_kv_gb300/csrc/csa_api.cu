@@ -55,6 +55,13 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     if (w.splits > 1) off = align_up(off + Tz * w.splits * w.H * kHD * 4, A);
     w.off_part_ml = off;
     if (w.splits > 1) off = align_up(off + Tz * w.splits * w.H * 2 * 4, A);
+    // the decode indexer's folded selection: one candidate slot per (token,
+    // CTA owning part of it), at most grid + tokens of them (sized for up to
+    // kFusedMaxTokens tokens, so the size only grows with T)
+    w.fslots = kMaxIdxCtas + static_cast<int32_t>(Tz < size_t(kFusedMaxTokens) ? Tz : kFusedMaxTokens);
+    w.fcap = 2 * p.top_k + 96;
+    w.off_fcand = off;   off = align_up(off + size_t(w.fslots) * w.fcap * 8, A);
+    w.off_fmeta = off;   off = align_up(off + size_t(w.fslots) * 16, A);
     w.data_bytes = off;
     w.total = w.state_bytes + w.data_bytes + A;
     return w;
@@ -218,6 +225,12 @@ csa_status_t csa_workspace_size(const csa_layout_t *layout, const csa_params_t *
     return CSA_OK;
 }
 
+// Tokens are scored one per key tile (decode batches): the prefill grouping
+// of four tokens of one sequence per tile does not apply.
+static bool one_token_per_tile(const csa_layout_t &L) {
+    return !(L.num_seqs == 1 && L.num_tokens >= 4);
+}
+
 static csa_status_t indexer_scores_impl(const csa_layout_t *layout, const csa_params_t *params,
                                         const void *q_idx, const float *w_idx, const void *k_idx,
                                         float *scores, int64_t ld_scores, int32_t *dev_status,
@@ -232,6 +245,9 @@ static csa_status_t indexer_scores_impl(const csa_layout_t *layout, const csa_pa
     int sms = 0;
     CSA_TRY(current_device(&sms));
     Launch lc{static_cast<cudaStream_t>(stream), sms};
+    if (!fp4 && one_token_per_tile(*layout) && decode_indexer_fits(*layout, sms, false))
+        return cuda_status(launch_decode_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores,
+                                                 ld_scores, dev_status, nullptr));
     return cuda_status(launch_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores,
                                       ld_scores, nullptr, dev_status, fp4));
 }
@@ -333,6 +349,55 @@ csa_status_t csa_sparse_mqa_decode(int32_t num_tokens, const csa_params_t *param
                                         dev_status));
 }
 
+// Steps 1 and 2: the selection of every token into idx / nsel.  Decode
+// batches go through the decode indexer with the selection folded in; other
+// layouts (prefill chunks, FP4 keys, very large batches) through the indexer
+// and the separate top-k.
+static cudaError_t select_blocks(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
+                                 const WsPlan &plan, uint8_t *w, uint32_t *state,
+                                 const void *q_idx, const float *w_idx, const void *k_idx,
+                                 int32_t *idx, int32_t *nsel, int32_t *dev_status, bool fp4) {
+    float *scores = reinterpret_cast<float *>(w + plan.off_scores);
+    if (!fp4 && one_token_per_tile(L) && decode_indexer_fits(L, lc.sm_count, true)) {
+        FusedTopk f;
+        f.state = state;
+        f.cand = reinterpret_cast<uint64_t *>(w + plan.off_fcand);
+        f.meta = reinterpret_cast<uint4 *>(w + plan.off_fmeta);
+        f.slots = plan.fslots;
+        f.cap = plan.fcap;
+        f.idx = idx;
+        f.n_sel = nsel;
+        return launch_decode_indexer(lc, L, p, q_idx, w_idx, k_idx, scores, plan.ld, dev_status, &f);
+    }
+    const bool fuse = indexer_fuses_hist(L);
+    cudaError_t e = launch_indexer(lc, L, p, q_idx, w_idx, k_idx, scores, plan.ld,
+                                   fuse ? state : nullptr, dev_status, fp4);
+    if (e != cudaSuccess) return e;
+    TopkWs tw{state, reinterpret_cast<uint64_t *>(w + plan.off_slots),
+              reinterpret_cast<uint32_t *>(w + plan.off_slot_cnt)};
+    return launch_topk(lc, L, p, scores, plan.ld, tw, fuse, idx, nsel, dev_status);
+}
+
+csa_status_t csa_indexer_topk(const csa_layout_t *layout, const csa_params_t *params,
+                              const void *q_idx, const float *w_idx, const void *k_idx,
+                              int32_t *idx, int32_t *n_sel, int32_t *dev_status, void *ws,
+                              size_t ws_bytes, void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, false));
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!q_idx || !w_idx || !idx || !n_sel || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (layout->total_comp_rows > 0 && !k_idx) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q_idx) || (k_idx && !aligned16(k_idx))) return CSA_ERR_INVALID_ARGUMENT;
+    const WsPlan plan = make_plan(layout->num_tokens, layout->max_comp_rows, *params);
+    CSA_TRY(check_ws(plan, ws, ws_bytes));
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    uint8_t *w = data_base(ws, ws_bytes, plan);
+    return cuda_status(select_blocks(lc, *layout, *params, plan, w, static_cast<uint32_t *>(ws),
+                                     q_idx, w_idx, k_idx, idx, n_sel, dev_status, false));
+}
+
 static csa_status_t decode_impl(const csa_layout_t *layout, const csa_params_t *params,
                                 const void *q_idx, const float *w_idx, const void *k_idx,
                                 const void *comp_kv, const void *q, const float *sinks, float *out,
@@ -352,17 +417,11 @@ static csa_status_t decode_impl(const csa_layout_t *layout, const csa_params_t *
     CSA_TRY(current_device(&sms));
     Launch lc{static_cast<cudaStream_t>(stream), sms};
     uint8_t *w = data_base(ws, ws_bytes, plan);
-    float *scores = reinterpret_cast<float *>(w + plan.off_scores);
     uint32_t *state = static_cast<uint32_t *>(ws);
     int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(w + plan.off_idx);
     int32_t *nsel = reinterpret_cast<int32_t *>(w + plan.off_nsel);
-    const bool fuse = indexer_fuses_hist(*layout);
-    cudaError_t e = launch_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores, plan.ld,
-                                   fuse ? state : nullptr, dev_status, fp4);
-    if (e != cudaSuccess) return CSA_ERR_CUDA;
-    TopkWs tw{state, reinterpret_cast<uint64_t *>(w + plan.off_slots),
-              reinterpret_cast<uint32_t *>(w + plan.off_slot_cnt)};
-    e = launch_topk(lc, *layout, *params, scores, plan.ld, tw, fuse, idx, nsel, dev_status);
+    cudaError_t e = select_blocks(lc, *layout, *params, plan, w, state, q_idx, w_idx, k_idx, idx,
+                                  nsel, dev_status, fp4);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     RowSource R{};
     R.fused = kRowsSelected;

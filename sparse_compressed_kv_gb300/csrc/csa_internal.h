@@ -20,6 +20,15 @@ constexpr int kHeadGroup = 16;   // query heads per attention CTA
 constexpr int kMaxFilterChunk = 4096;  // scores per top-k filter CTA (multi-CTA mode)
 constexpr int kMaxPerTok = 512;        // top-k filter CTAs per token
 
+// Decode indexer (one query token per key tile), with or without the top-k
+// folded in (csa_indexer_topk.cu).  Key ranges are cut in units of kBoxRows
+// keys (the TMA box height), so CTAs get equal shares to within one unit.
+constexpr int kBoxRows = 32;
+constexpr int kMaxIdxCtas = 192;       // grid cap of the decode indexer
+constexpr int kDecMaxTokens = 1024;    // tokens the decode indexer takes
+constexpr int kFusedMaxTokens = 512;   // tokens the fused selection takes
+constexpr int kSegKeysMax = 8192;      // keys one CTA keeps on chip for its local selection
+
 struct WsPlan {
     int64_t T = 0;
     int64_t ld = 0;          // row stride of the workspace score matrix
@@ -38,6 +47,9 @@ struct WsPlan {
     size_t state_bytes = 0;
     size_t off_scores = 0, off_slots = 0, off_slot_cnt = 0;   // offsets inside the data area
     size_t off_idx = 0, off_nsel = 0, off_part_o = 0, off_part_ml = 0;
+    size_t off_fcand = 0, off_fmeta = 0;  // fused selection: candidate slots and their headers
+    int32_t fslots = 0;                   // candidate slots (grid cap + tokens)
+    int32_t fcap = 0;                     // entries per candidate slot
     size_t data_bytes = 0;
     size_t total = 0;        // state + data + alignment slack
 };
@@ -68,6 +80,29 @@ struct TopkWs {
 
 // Shape of the top-k filter grid for T tokens of at most max_comp_rows blocks.
 void topk_grid(int64_t T, int64_t max_comp_rows, int32_t *chunk, int32_t *per_tok);
+
+// Fused selection of the decode indexer: where its candidates go and where
+// the selection lands (device pointers).
+struct FusedTopk {
+    uint32_t *state;       // [T][kStateWords] per-token state (its ticket word is used)
+    uint64_t *cand;        // [slots][cap] (key << 32 | block) candidates, ascending block
+    uint4 *meta;           // [slots] count, bound, overflow, length
+    int32_t slots, cap;
+    int32_t *idx;          // [T][top_k]
+    int32_t *n_sel;        // [T]
+};
+
+// The decode indexer (bf16 keys, one token per key tile) takes this layout:
+// at most kDecMaxTokens tokens; with the fused selection, at most
+// kFusedMaxTokens and at most kSegKeysMax keys per CTA.
+bool decode_indexer_fits(const csa_layout_t &L, int sm_count, bool fused);
+
+// Scores of every visible block (fused == nullptr), or the top-k selection
+// as well (scores then go to the workspace, for the exact fallback).
+cudaError_t launch_decode_indexer(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
+                                  const void *q_idx, const float *w_idx, const void *k_idx,
+                                  float *scores, int64_t ld, int32_t *status,
+                                  const FusedTopk *fused);
 
 // Where attention rows come from.
 enum RowMode { kRowsGathered = 0, kRowsSelected = 1, kRowsAllVisible = 2 };

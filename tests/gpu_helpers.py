@@ -105,6 +105,14 @@ class Run:
         self.check_guards()
         return idx, n_sel
 
+    def indexer_topk(self):
+        idx = self.buf((self.T, self.wl.top_k), torch.int32, -7)
+        n_sel = self.buf((self.T,), torch.int32, -7)
+        csa.csa_indexer_topk(self.layout, self.prm, self.d.q_idx, self.d.w_idx, self.d.k_idx, idx,
+                             n_sel, self.status, self.ws)
+        self.check_guards()
+        return idx, n_sel
+
     def gather(self, idx, n_sel):
         rows = self.wl.top_k + self.wl.window
         kv_buf = self.buf((self.T, rows, self.wl.hd), torch.bfloat16, 0)

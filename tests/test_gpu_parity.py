@@ -189,3 +189,75 @@ def test_host_errors_on_gpu(cuda_device):
         csa.csa_indexer_scores(run.layout, bad, run.d.q_idx, run.d.w_idx, run.d.k_idx,
                                torch.empty(1, 256, device=cuda_device), run.status)
     assert e.value.code == 2   # CSA_ERR_UNSUPPORTED
+
+
+def _monotone():
+    # every head's query is one direction v and block s's key is 2^(s/256) v:
+    # scores grow with the block index, so the whole selection sits in the
+    # last key range and the candidates of the other ranges cannot prove it
+    # (the selection then comes from the whole score row)
+    wl = W.make("monotone", seed=30, seq_lens=[4 * 2000], n_comp=[2000], top_k=100, n_heads=16)
+    g = torch.Generator().manual_seed(7)
+    v = torch.randn(wl.ihd, generator=g)
+    v = v / v.norm()
+    wl.q_idx[0] = v.to(torch.bfloat16)[None, :].expand(wl.n_ih, -1)
+    wl.w_idx.fill_(1.0 / 64)
+    c = torch.pow(2.0, torch.arange(2000, dtype=torch.float32) / 256.0)
+    wl.k_idx[:2000] = (c[:, None] * v[None, :]).to(torch.bfloat16)
+    return wl
+
+
+def _ties():
+    wl = W.make("ties2", seed=31, seq_lens=[4 * 2000], n_comp=[2000], top_k=100, n_heads=16)
+    base = wl.k_idx[:40].clone()
+    for rep in range(50):
+        wl.k_idx[40 * rep:40 * rep + 40] = base
+    return wl
+
+
+def _flat():
+    wl = W.make("flat2", seed=32, seq_lens=[4 * 20000], n_comp=[20000], top_k=1000, n_heads=16)
+    wl.w_idx.zero_()
+    return wl
+
+
+def _signs():
+    wl = W.make("signs2", seed=33, seq_lens=[4 * 3000], n_comp=[3000], top_k=300, n_heads=16)
+    wl.w_idx.copy_(-wl.w_idx.abs())
+    return wl
+
+
+INDEXER_TOPK_CASES = {
+    "tiny": lambda: W.tiny(seed=9),
+    "ragged": lambda: W.make("ragged2", seed=34, seq_lens=[4 * 300 + 3, 90, 4 * 1000 + 1],
+                             tokens=[1, 2, 1], n_comp=[300, 22, 1000], top_k=64, n_heads=16,
+                             swa_cap=160),
+    "batch": lambda: W.make("batch6", seed=35, seq_lens=[4 * n for n in
+                                                         [5000, 12000, 800, 30000, 2500, 64]],
+                            n_comp=[5000, 12000, 800, 30000, 2500, 64], top_k=512, n_heads=16),
+    "chunk": lambda: W.make("chunk2", seed=36, seq_lens=[4 * 700], tokens=[37], top_k=128,
+                            n_heads=16, swa_cap=256),
+    "ties": _ties, "flat": _flat, "signs": _signs, "monotone": _monotone,
+}
+
+
+@pytest.mark.parametrize("name", list(INDEXER_TOPK_CASES))
+def test_indexer_topk_equals_topk_on_the_scores(cuda_device, name):
+    """csa_indexer_topk (the selection folded into the indexer for decode
+    batches) selects exactly what csa_topk selects on csa_indexer_scores'
+    scores, which is the oracle's selection on those scores, and again on a
+    second call with the same workspace."""
+    wl = INDEXER_TOPK_CASES[name]()
+    run = H.Run(wl, cuda_device)
+    sc = run.scores()
+    ref_idx, ref_n = run.topk(sc)
+    H.check_topk_exact(wl, sc, ref_idx, ref_n)
+    for _ in range(2):
+        idx, n_sel = run.indexer_topk()
+        torch.cuda.synchronize()
+        assert torch.equal(n_sel, ref_n)
+        assert torch.equal(idx, ref_idx)
+    if name == "monotone":
+        # the selection is the tail of the cache (rounding may swap neighbours)
+        assert idx.cpu().numpy()[0].min() >= 1800
+    assert run.dev_status() == 0
