@@ -35,19 +35,20 @@ METRIC = "CSA decode tokens/s per layer at 1M ctx (batch 1 & 32); % of HBM/tenso
 UNIT = "tokens/s/layer"
 
 
-# DRAM bytes (read + write) of one indexer launch on the 1M workload, from the
+# DRAM bytes (read + write) of one launch of the step's dominant kernel (the
+# decode indexer with the top-k folded in) on the 1M workload, from the
 # committed ncu capture of that step (profiles/), and the SHA-256 prefix of the
 # kernel source it was taken on: once the source changes the figure no longer
 # describes the kernel, and the roofline reports traffic null.
-INDEXER_TRAFFIC_BYTES = 67166208 + 459776
-INDEXER_TRAFFIC_SOURCE = "bcc0dfdaa0a2df58"
+SELECT_TRAFFIC_BYTES = None
+SELECT_TRAFFIC_SOURCE = ""
 
 
-def indexer_traffic():
+def select_traffic():
     import hashlib
-    src = os.path.join(ROOT, "sparse_compressed_kv_gb300", "csrc", "csa_indexer.cu")
+    src = os.path.join(ROOT, "sparse_compressed_kv_gb300", "csrc", "csa_indexer_topk.cu")
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return INDEXER_TRAFFIC_BYTES if h == INDEXER_TRAFFIC_SOURCE else None
+    return SELECT_TRAFFIC_BYTES if h == SELECT_TRAFFIC_SOURCE else None
 
 
 def peaks():
@@ -436,8 +437,25 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     res0 = (layers[0].idx[0].cpu().numpy().copy(), layers[0].out[0].cpu().numpy().copy())
 
-    # ---- the dominant kernel alone (indexer): one graph holds one launch per
-    # rotating layer, so replays carry no host overhead; CUDA events on `stream`
+    # ---- the dominant kernel alone (the indexer with the top-k folded in, as
+    # the step runs it): one graph holds one launch per rotating layer, so
+    # replays carry no host overhead; CUDA events on `stream`
+    nsel_buf = torch.empty(wl0.num_tokens, dtype=torch.int32, device=device)
+
+    def select_all():
+        for L in layers:
+            csa.csa_indexer_topk(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, L.idx, nsel_buf,
+                                 status, ws, stream=stream)
+    with torch.cuda.stream(stream):
+        select_all()
+    torch.cuda.synchronize()
+    sgraph = capture(select_all, stream)
+    reps = max(1, args.steps // len(layers))
+    sel_blocks = [time_graphs([sgraph], reps, max(1, args.warmup // len(layers)), stream)
+                  / len(layers) for _ in range(args.blocks)]
+    sel_ms = statistics.median(sel_blocks)
+
+    # ---- the indexer's scores alone (the same kernel without the selection)
     sc_buf = torch.empty(1, wl0.max_comp_rows, dtype=torch.float32, device=device)
 
     def index_all():
@@ -448,7 +466,6 @@ def run_ours(args, rank, world, device):
         index_all()
     torch.cuda.synchronize()
     igraph = capture(index_all, stream)
-    reps = max(1, args.steps // len(layers))
     idx_blocks = [time_graphs([igraph], reps, max(1, args.warmup // len(layers)), stream)
                   / len(layers) for _ in range(args.blocks)]
     idx_ms = statistics.median(idx_blocks)
@@ -581,7 +598,8 @@ def run_ours(args, rank, world, device):
                                                     tf_peak, peak_kind)
 
     tok_s = world * 1e3 / ms
-    achieved = ab["indexer"] / (idx_ms * 1e-3) / 1e9
+    achieved = ab["indexer"] / (sel_ms * 1e-3) / 1e9
+    idx_achieved = ab["indexer"] / (idx_ms * 1e-3) / 1e9
     n_vis0 = ab["keys"] // (wl0.ihd * 2)
     line = {
         "metric": METRIC, "value": round(tok_s, 1), "unit": UNIT, "n_gpus": world,
@@ -596,12 +614,18 @@ def run_ours(args, rank, world, device):
                          f"({args.layers * 0.34:.1f} GB) rotated, no flush",
                    "parallelism": f"replicas x{world}",
                    "graph": f"one CUDA graph per {len(layers)} steps (one per rotating layer)"},
-        "roofline": {"bound": "hbm", "kernel": "indexer (tcgen05, TMA)",
+        "roofline": {"bound": "hbm", "kernel": "indexer + top-k (csa_indexer_topk: tcgen05, TMA)",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": indexer_traffic(),
-                     "peak_kind": peak_kind, "kernel_ms": round(idx_ms, 5),
-                     "kernel_ms_blocks": spread(idx_blocks),
+                     "frac": round(achieved / hbm_peak, 4), "traffic": select_traffic(),
+                     "peak_kind": peak_kind, "kernel_ms": round(sel_ms, 5),
+                     "kernel_ms_blocks": spread(sel_blocks),
                      "bytes_per_launch": ab["indexer"]},
+        "indexer_scores_alone": {"kernel": "the same indexer without the selection "
+                                           "(csa_indexer_scores)",
+                                 "achieved": round(idx_achieved, 1), "unit": "GB/s",
+                                 "frac": round(idx_achieved / hbm_peak, 4),
+                                 "kernel_ms": round(idx_ms, 5),
+                                 "kernel_ms_blocks": spread(idx_blocks)},
         "indexer_keys_per_s": round(n_vis0 / (idx_ms * 1e-3), 1),
         "step_roofline": {"bound": "hbm", "algorithmic_bytes": ab["step"],
                           "achieved": round(ab["step"] / (ms * 1e-3) / 1e9, 1),

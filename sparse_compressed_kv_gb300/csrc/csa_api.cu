@@ -21,26 +21,22 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     w.H = p.n_heads;
     w.ld = ((max_comp_rows > 0 ? max_comp_rows : 1) + 3) / 4 * 4;
     topk_grid(T, max_comp_rows, &w.topk_chunk, &w.topk_per_tok);
-    // Attention split: enough CTAs for ~2 waves, at most 64 splits per token.
+    // Attention: a token's row slots (the window starts at a multiple of 4)
+    // in chunks of kTcChunk; splits per token so that about one CTA per SM
+    // runs, at most 64 (the combine's limit), each a whole number of chunks.
     const int64_t rows_max =
         rows_max_in >= 0 ? rows_max_in : static_cast<int64_t>(p.top_k) + p.window;
-    const int64_t chunks = (rows_max + kAttnChunk - 1) / kAttnChunk;
-    const int64_t ctas = (T > 0 ? T : 1) * (p.n_heads / kHeadGroup);
-    int64_t splits = (kTargetCtas + ctas - 1) / ctas;
+    const int64_t comp_max = rows_max > p.window ? rows_max - p.window : 0;
+    const int64_t slots = ((comp_max + 3) & ~int64_t(3)) + p.window;
+    const int64_t chunks = (slots + kTcChunk - 1) / kTcChunk;
+    const int64_t groups = (p.n_heads + kTcHeads - 1) / kTcHeads;
+    int64_t splits = kAttnCtas / ((T > 0 ? T : 1) * groups);
     if (splits > chunks) splits = chunks;
     if (splits > 64) splits = 64;
-    if (splits < (chunks + 63) / 64) splits = (chunks + 63) / 64;
     if (splits < 1) splits = 1;
     const int64_t per = (chunks + splits - 1) / splits;
-    w.rows_split = static_cast<int32_t>(per * kAttnChunk);
-    w.splits = static_cast<int32_t>((rows_max + w.rows_split - 1) / w.rows_split);
-    // When a token's splits fit one portable cluster (at most 8 CTAs), they
-    // merge their partials through distributed shared memory and write the
-    // output: no partials in global memory and no combine kernel.  With more
-    // splits the partials go through L2 to the combine: on-chip exchange of
-    // that volume is no faster than L2, and a merge per cluster would only
-    // add a step.
-    w.attn_cluster = (w.splits >= 2 && w.splits <= 8) ? w.splits : 1;
+    w.rows_split = static_cast<int32_t>(per * kTcChunk);
+    w.splits = static_cast<int32_t>((slots + w.rows_split - 1) / w.rows_split);
     const size_t A = 256;
     const size_t Tz = static_cast<size_t>(T > 0 ? T : 0);
     w.state_bytes = Tz * kStateWords * 4;
@@ -343,7 +339,7 @@ csa_status_t csa_sparse_mqa_decode(int32_t num_tokens, const csa_params_t *param
     R.kv_len = kv_len;
     R.rows_per_token = params->top_k + params->window;
     uint8_t *w = data_base(ws, ws_bytes, plan);
-    return cuda_status(launch_attention(lc, R, num_tokens, *params, plan, q, sinks, out,
+    return cuda_status(launch_attention_tc(lc, R, num_tokens, *params, plan, q, sinks, out,
                                         reinterpret_cast<float *>(w + plan.off_part_o),
                                         reinterpret_cast<float *>(w + plan.off_part_ml),
                                         dev_status));
@@ -433,7 +429,7 @@ static csa_status_t decode_impl(const csa_layout_t *layout, const csa_params_t *
     R.idx = idx;
     R.n_sel = nsel;
     R.comp_kv = comp_kv;
-    return cuda_status(launch_attention(lc, R, layout->num_tokens, *params, plan, q, sinks, out,
+    return cuda_status(launch_attention_tc(lc, R, layout->num_tokens, *params, plan, q, sinks, out,
                                         reinterpret_cast<float *>(w + plan.off_part_o),
                                         reinterpret_cast<float *>(w + plan.off_part_ml),
                                         dev_status, true));
@@ -493,7 +489,7 @@ csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *para
     R.window = params->window;
     R.top_k = params->top_k;
     R.comp_kv = comp_kv;
-    return cuda_status(launch_attention(lc, R, layout->num_tokens, *params, plan, q, sinks, out,
+    return cuda_status(launch_attention_tc(lc, R, layout->num_tokens, *params, plan, q, sinks, out,
                                         reinterpret_cast<float *>(w + plan.off_part_o),
                                         reinterpret_cast<float *>(w + plan.off_part_ml),
                                         dev_status));

@@ -1,0 +1,687 @@
+// csa_attention_tc.cu -- shared-KV multi-query attention on the 5th-generation
+// tensor cores, all of a token's query heads (up to 64) in one CTA.
+//
+//   l_j = scale * q_h . row_j,   out_h = sum_j softmax_j(l) row_j
+//
+// ("ARCHITECTURE & MEMORY AUDIT -- 1M-context viability", D5 and D6: every
+// 512-wide row is the key and the value of all query heads; M5: the selected
+// compressed rows are read by index, the window rows from the ring, with no
+// gather buffer.  "PART A -- Next Session Clues", section 3: both kept where
+// they overlap.)
+//
+// A CTA owns one token, up to 64 heads and a contiguous range of the token's
+// row slots, which it walks in chunks of 64 rows.  Each row is read once for
+// all of the CTA's heads:
+//   warp 1      TMEM allocator + tcgen05.mma issuer:
+//                 S  = Q . rows^T       M = 64 heads, N = 64 rows, K = 512
+//                 O^T += rows^T . P^T   M = 128 of the 512 columns (the row
+//                                       tile read MN-major), N = 64 heads,
+//                                       K = 64 rows; P as two bf16 terms
+//   warps 0, 6+ fetch a chunk's rows by index into a two-stage ring (16-byte
+//               cp.async, 512 contiguous bytes per warp instruction, placed
+//               in the 128-byte-swizzled layout the MMA reads); a chunk is
+//               handed to the MMA as soon as it has landed
+//   warps 2..5  online softmax: two lanes per head (the M = 64 accumulator's
+//               row h sits in lane h % 16 of lane quarter h / 16; its upper
+//               32 columns go to the lane 16 above), then the epilogue (one
+//               output column per lane).
+// S is double-buffered in TMEM and the MMA warp issues QK^T of chunk i+1
+// before PV of chunk i, so it runs during the softmax of chunk i; O^T
+// accumulates in TMEM across chunks.  Exponentials use the
+// running maximum of each head; when a chunk raises it by more than 8 (log2
+// units) the accumulated O^T and l are rescaled first, so a weight never
+// exceeds 2^8 and the two bf16 terms of P keep ~16 bits of it.
+//
+// Row slots of a token: its selected compressed rows (or, HCA, every visible
+// block) first, then its window rows starting at the next multiple of 4,
+// padding masked.  With several splits per token
+// each CTA writes its partial (O, m, l) and a combine kernel merges them.
+#include <math.h>
+
+#include "csa_device.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+namespace {
+
+#ifndef CSA_TC_LOAD_WARPS
+#define CSA_TC_LOAD_WARPS 4
+#endif
+constexpr int kLdWarps = CSA_TC_LOAD_WARPS;    // row-fetch warps: warp 0 and warps 6 ..
+constexpr int kLdRows = 64 / kLdWarps;         // rows of a chunk per fetch warp
+constexpr int kTcWarps = 5 + kLdWarps;
+constexpr int kTcThreads = 32 * kTcWarps;
+constexpr int kSmThreads = 128;                // warps 2..5
+constexpr int kBarSm = 1;                      // named barrier of the softmax warps
+constexpr int kLdThreads = 32 * kLdWarps;
+constexpr int kHG = 64;                        // heads per CTA (MMA M of QK^T)
+constexpr int kChunk = 64;                     // rows per chunk (QK^T N, PV K)
+constexpr int kQBytes = 8 * kHG * 128;         // 64 KiB: Q, eight 64-column boxes
+constexpr int kRowBox = kChunk * 128;          // 8 KiB: 64 columns of a chunk's rows
+constexpr int kRowsBytes = 8 * kRowBox;        // 64 KiB per stage
+constexpr int kPBytes = kHG * kChunk * 2;      // 8 KiB: one bf16 term of P
+constexpr int kTmemCols = 512;
+constexpr int kSCol = 0;                       // S buffers: columns 0 .. 127
+constexpr int kOCol = 128;                     // O^T: 4 tiles x 64 heads
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleAbove = 8.f;           // log2 units
+
+struct TcParams {
+    RowSource R;
+    int32_t H;
+    int32_t splits;
+    int32_t rows_split;      // slots per split, a multiple of kChunk
+    float scale_log2;
+    const float *sinks;      // [H] or null
+    float *out;              // [T][H][512]
+    float *part_o;           // [T][splits][H][512]
+    float *part_ml;          // [T][splits][H][2]  (m in log2 units, l)
+    int32_t *status;
+    int32_t early_q;
+};
+
+struct TcTok;
+
+struct TcSmem {
+    uint32_t maskw[2][kLdWarps];   // valid rows of the chunk in each stage, per fetch warp
+    uint64_t q_full;
+    uint64_t full[2], empty[2];
+    uint64_t sfull[2], sfree[2];
+    uint64_t pfull[2], pfree[2];
+    uint64_t odone;
+    float alpha[kHG];        // rescale factors of the current chunk
+    float fin[kHG];          // output scale per head
+    float mh[kHG], lh[kHG];
+    uint32_t flag[2][4];     // per chunk parity: heads of each warp that rescale
+    uint32_t tmem_holder;
+    int32_t nslots;          // the token's row slots
+};
+
+// Row slots of token t: selected (or every visible) compressed rows first, then
+// the window rows from the next multiple of 4.  Fills the counts; returns the
+// slot count.
+struct TcTok {
+    int32_t nsel;      // compressed rows
+    int32_t nswa;      // window rows
+    int32_t wslot;     // first window slot
+    int64_t first;     // first window position
+    int64_t off;       // the sequence's first cache row
+    int64_t n_vis;
+    int64_t first_res;  // oldest position the ring holds
+    int b;
+    int bad;
+    int32_t gathered_len;
+};
+
+__device__ __forceinline__ TcTok tc_token(const RowSource &R, int t) {
+    TcTok k{};
+    if (R.fused == kRowsGathered) {
+        int32_t len = R.kv_len[t];
+        if (len < 0 || len > R.rows_per_token) {
+            k.bad = CSA_DEV_BAD_LENGTH;
+            len = len < 0 ? 0 : R.rows_per_token;
+        }
+        k.gathered_len = len;
+        k.nsel = len;
+        k.wslot = len;
+        return k;
+    }
+    const int32_t ns_sel = R.fused == kRowsSelected ? R.n_sel[t] : 0;
+    const TokenView v = token_view(R.L, R.ratio, t);
+    k.bad = v.bad;
+    if (v.bad & CSA_DEV_BAD_LAYOUT) return k;
+    int32_t ns;
+    if (R.fused == kRowsAllVisible) {
+        ns = static_cast<int32_t>(v.n_vis);
+    } else {
+        ns = ns_sel;
+        if (ns < 0 || ns > R.top_k) {
+            k.bad |= CSA_DEV_BAD_LENGTH;
+            ns = ns < 0 ? 0 : R.top_k;
+        }
+    }
+    k.nsel = ns;
+    k.wslot = (ns + 3) & ~3;
+    k.first = window_first(v.pos, R.window);
+    k.nswa = static_cast<int32_t>(v.pos - k.first + 1);
+    k.off = v.off;
+    k.n_vis = v.n_vis;
+    k.b = v.b;
+    k.first_res = R.L.swa_first_pos[v.b];
+    return k;
+}
+
+__device__ __forceinline__ void tmem_ld16_raw(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16_raw(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// 2^x with the hardware's approximate exponential (relative error about
+// 2^-22, far below the bf16 terms P is stored in); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory descriptor with explicit leading / stride byte offsets
+// (128-byte swizzle).  K-major: the stride is the step between 8-row groups.
+// MN-major: the leading offset is the step between 64-element column boxes,
+// the stride the step between 8-row groups of the K dimension.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// kind::f16, bf16 x bf16 -> f32, M x N, A transposed (MN-major) or not.
+template <int M, int N, bool kTransA>
+__device__ __forceinline__ constexpr uint32_t idesc_bf16() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((kTransA ? 1u : 0u) << 15) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attention_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const TcParams A) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_smem<1024>(smem_raw);
+    uint8_t *sQ = smem;
+    uint8_t *sRows = smem + kQBytes;                       // [2][8 boxes][64 rows][128 B]
+    uint8_t *sP = sRows + 2 * kRowsBytes;                  // [2 buffers][hi, lo][64 heads][128 B]
+    TcSmem &S = *reinterpret_cast<TcSmem *>(sP + 4 * kPBytes);
+
+    const int split = blockIdx.x, hg = blockIdx.y, t = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h0 = hg * kHG;
+    const int H = A.H;
+
+    if (tid == 0) {
+        mbar_init(&S.q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&S.full[i], kLdThreads);
+            mbar_init(&S.empty[i], 1);
+            mbar_init(&S.sfull[i], 1);
+            mbar_init(&S.sfree[i], kSmThreads);
+            mbar_init(&S.pfull[i], kSmThreads);
+            mbar_init(&S.pfree[i], 1);
+        }
+        mbar_init(&S.odone, 1);
+        mbar_fence_init();
+        tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(&S.tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_holder;
+
+    // Q of this token's head group: eight 64 x 64 boxes (heads past H read the
+    // next token's rows or the tensor's zero fill; their outputs are dropped)
+    auto load_q = [&]() {
+        mbar_arrive_expect_tx(&S.q_full, kQBytes);
+        const int y = t * H + h0;
+        for (int bx = 0; bx < 8; ++bx)
+            tma_load_2d(sQ + bx * (kHG * 128), &tm_q, bx * 64, y, &S.q_full, policy_evict_normal());
+    };
+    if (A.early_q && tid == 0) load_q();
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!A.early_q && tid == 0) load_q();
+
+    // the token's row slots (one reader, shared)
+    __shared__ TcTok tok_s;
+    if (tid == 0) {
+        const TcTok kk = tc_token(A.R, t);
+        tok_s = kk;
+        S.nslots = A.R.fused == kRowsGathered ? kk.gathered_len : kk.wslot + kk.nswa;
+        if (split == 0 && hg == 0) raise_status(A.status, kk.bad);
+    }
+    __syncthreads();
+    const int nslots = S.nslots;
+    const int s_begin = split * A.rows_split;
+    const int s_end = min(nslots, s_begin + A.rows_split);
+    const int nch = s_end > s_begin ? (s_end - s_begin + kChunk - 1) / kChunk : 0;
+
+    if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0 && nch > 0) {
+            mbar_wait(&S.q_full, 0, A.status);
+            constexpr uint32_t id_qk = idesc_bf16<kHG, kChunk, false>();
+            constexpr uint32_t id_pv = idesc_bf16<128, kHG, true>();
+            const uint32_t q_base = smem_addr(sQ);
+            const uint32_t r_base = smem_addr(sRows);
+            const uint32_t p_base = smem_addr(sP);
+            // S = Q . rows^T of chunk i, into S buffer i % 2
+            auto qk = [&](int i) {
+                const int st = i & 1;
+                const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
+                mbar_wait(&S.full[st], ph, A.status);
+                mbar_wait(&S.sfree[st], ph ^ 1u, A.status);
+                tc_fence_after();
+                const uint32_t rows = r_base + st * kRowsBytes;
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk) {
+                    const uint32_t bx = kk >> 2, ko = (kk & 3) * 32;
+                    umma_bf16(tmem + kSCol + st * kChunk,
+                              sw128_desc(q_base + bx * (kHG * 128) + ko, 16, 1024),
+                              sw128_desc(rows + bx * kRowBox + ko, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&S.sfull[st]);
+            };
+            // QK^T of the next chunk goes out before PV of this one, so it
+            // runs while the softmax of this chunk does
+            qk(0);
+            for (int i = 0; i < nch; ++i) {
+                if (i + 1 < nch) qk(i + 1);
+                const int st = i & 1;
+                const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
+                const uint32_t rows = r_base + st * kRowsBytes;
+                mbar_wait(&S.pfull[st], ph, A.status);
+                tc_fence_after();
+                // O^T[d][h] += sum_j rows[j][d] P[h][j], per 128-column tile of d
+                const uint32_t pb = p_base + st * 2 * kPBytes;
+#pragma unroll
+                for (int dt = 0; dt < 4; ++dt)
+#pragma unroll
+                    for (int ks = 0; ks < kChunk / 16; ++ks) {
+                        const uint64_t adesc =
+                            sw128_desc(rows + (2 * dt) * kRowBox + ks * 16 * 128, kRowBox, 1024);
+                        const uint32_t acc0 = (i > 0 || ks > 0) ? 1u : 0u;
+                        umma_bf16(tmem + kOCol + dt * kHG, adesc, sw128_desc(pb + ks * 32, 16, 1024),
+                                  id_pv, acc0);
+                        umma_bf16(tmem + kOCol + dt * kHG, adesc,
+                                  sw128_desc(pb + kPBytes + ks * 32, 16, 1024), id_pv, 1u);
+                    }
+                umma_commit(&S.empty[st]);
+                umma_commit(&S.pfree[st]);
+            }
+            umma_commit(&S.odone);
+        }
+    } else if (warp == 0 || warp >= 6) {
+        // ------------------------------------------------ row fetch
+        const TcTok k = tok_s;
+        const int li = warp == 0 ? 0 : warp - 5;   // rows kLdRows li .. of each chunk
+        const void *dummy = A.R.fused == kRowsGathered ? A.R.kv_buf : A.R.L.swa_kv;
+        int bad = 0;
+        // lane r < kLdRows resolves row r of the warp's share, then the warp
+        // copies row after row, 512 contiguous bytes per instruction
+        auto issue = [&](int i) {
+            const int st = i & 1;
+            const int j = s_begin + i * kChunk + kLdRows * li + lane;
+            const __nv_bfloat16 *src = nullptr;
+            if (lane < kLdRows && j < s_end) {
+                if (A.R.fused == kRowsGathered) {
+                    src = static_cast<const __nv_bfloat16 *>(A.R.kv_buf) +
+                          (static_cast<int64_t>(t) * A.R.rows_per_token + j) * kHD;
+                } else if (j < k.nsel) {
+                    const int32_t sidx = A.R.fused == kRowsAllVisible
+                                             ? j
+                                             : A.R.idx[static_cast<int64_t>(t) * A.R.top_k + j];
+                    if (sidx < 0 || sidx >= k.n_vis) bad |= CSA_DEV_BAD_INDEX;
+                    else src = static_cast<const __nv_bfloat16 *>(A.R.comp_kv) + (k.off + sidx) * kHD;
+                } else if (j >= k.wslot) {
+                    const int64_t x = k.first + (j - k.wslot);
+                    if (x < k.first_res) bad |= CSA_DEV_MISSING_SWA;
+                    else
+                        src = static_cast<const __nv_bfloat16 *>(A.R.L.swa_kv) +
+                              (static_cast<int64_t>(k.b) * A.R.L.swa_cap + x % A.R.L.swa_cap) * kHD;
+                }
+            }
+            const uint32_t okm = __ballot_sync(0xffffffffu, src != nullptr);
+            if (lane == 0) S.maskw[st][li] = okm;
+            uint8_t *rows = sRows + st * kRowsBytes;
+#pragma unroll 4
+            for (int rr = 0; rr < kLdRows; ++rr) {
+                const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(__shfl_sync(
+                    0xffffffffu, reinterpret_cast<unsigned long long>(src), rr));
+                const int row = kLdRows * li + rr;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int c = lane + 32 * u;   // 16-byte piece of the row
+                    uint8_t *dst = rows + (c >> 3) * kRowBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                    cp_async16(dst, p ? static_cast<const void *>(p + c * 8) : dummy, p != nullptr);
+                }
+            }
+            cp_async_commit();
+        };
+        // chunk i + 1 is handed over as soon as it has landed; chunk i + 2
+        // goes into the stage of chunk i once PV of chunk i is done with it
+        if (nch > 0) issue(0);
+        if (nch > 1) {
+            issue(1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        if (nch > 0) {
+            fence_proxy_async_smem();
+            mbar_arrive(&S.full[0]);
+        }
+        for (int i = 0; i < nch; ++i) {
+            if (i + 1 < nch) {
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+                mbar_arrive(&S.full[(i + 1) & 1]);
+            }
+            if (i + 2 < nch) {
+                mbar_wait(&S.empty[i & 1], static_cast<uint32_t>(i >> 1) & 1u, A.status);
+                issue(i + 2);
+            }
+        }
+        bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(bad)));
+        if (lane == 0) raise_status(A.status, bad);
+    } else if (warp >= 2) {
+        // ------------------------------------------------ softmax, epilogue
+        const int q = warp & 3;                  // TMEM lane quarter
+        const int hl = q * 16 + (lane & 15);     // head of this lane (two lanes per head)
+        const bool upper = lane >= 16;           // rows 32..63 of the chunk
+        const bool hv = h0 + hl < H;
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        float m_ref = -INFINITY, l = 0.f;
+        const int st_t = tid - 64;
+        for (int i = 0; i < nch; ++i) {
+            const int st = i & 1;
+            const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
+            mbar_wait(&S.sfull[st], ph, A.status);
+            tc_fence_after();
+            uint32_t sr[4][16];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) tmem_ld16_raw(tmem + lane_off + kSCol + st * kChunk + c4 * 16, sr[c4]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&S.sfree[st]);
+            mbar_wait(&S.full[st], ph, A.status);   // orders the fetch warps' mask writes
+            uint64_t msk = 0;
+#pragma unroll
+            for (int w = 0; w < kLdWarps; ++w) msk |= static_cast<uint64_t>(S.maskw[st][w]) << (kLdRows * w);
+            // lane l < 16 takes rows 0..31 of head hl, lane l + 16 rows 32..63
+            float x[32];
+            float mc = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint32_t hi = __shfl_sync(0xffffffffu, sr[2 + (j >> 4)][j & 15], lane & 15);
+                const uint32_t v = upper ? hi : sr[j >> 4][j & 15];
+                const int row = (upper ? 32 : 0) + j;
+                x[j] = (msk >> row) & 1ull ? __uint_as_float(v) * A.scale_log2 : -INFINITY;
+                mc = fmaxf(mc, x[j]);
+            }
+            mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
+            // a head whose maximum rises by more than kRescaleAbove rescales
+            // what it has accumulated (every lane of the four warps takes part)
+            const bool need = hv && m_ref != -INFINITY && mc > m_ref + kRescaleAbove;
+            const uint32_t wneed = __ballot_sync(0xffffffffu, need);
+            if (lane == 0) S.flag[st][q] = wneed;
+            float alpha = 1.f;
+            if (need) {
+                alpha = exp2f(m_ref - mc);
+                m_ref = mc;
+                l *= alpha;
+            } else if (m_ref == -INFINITY) {
+                m_ref = mc;
+            }
+            named_bar_sync(kBarSm, kSmThreads);
+            const bool any = (S.flag[st][0] | S.flag[st][1] | S.flag[st][2] | S.flag[st][3]) != 0;
+            if (any) {
+                if (!upper) S.alpha[hl] = alpha;
+                // PV of the previous chunk must have landed in O^T
+                mbar_wait(&S.pfree[st ^ 1], static_cast<uint32_t>((i - 1) >> 1) & 1u, A.status);
+                named_bar_sync(kBarSm, kSmThreads);
+                tc_fence_after();
+#pragma unroll 1
+                for (int dt = 0; dt < 4; ++dt)
+#pragma unroll 1
+                    for (int hb = 0; hb < 4; ++hb) {
+                        uint32_t r[16];
+                        const uint32_t ta = tmem + lane_off + kOCol + dt * kHG + hb * 16;
+                        tmem_ld16_raw(ta, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            r[c] = __float_as_uint(__uint_as_float(r[c]) * S.alpha[hb * 16 + c]);
+                        tmem_st16_raw(ta, r);
+                    }
+                tmem_wait_st();
+                tc_fence_before();
+                named_bar_sync(kBarSm, kSmThreads);
+            }
+            // P = 2^(x - m_ref) as hi + lo bf16 terms, this lane's half of row hl
+            // (a head with no valid row yet keeps m_ref = -inf; its masked
+            // logits must give 0, not 2^(-inf + inf))
+            const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+            float sum = 0.f;
+            uint32_t phi[16], plo[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float p0 = fast_exp2(x[j] - mr);
+                const float p1 = fast_exp2(x[j + 1] - mr);
+                sum += p0 + p1;
+                const __nv_bfloat162 hi2 = __floats2bfloat162_rn(p0, p1);
+                const float2 hf = __bfloat1622float2(hi2);
+                const __nv_bfloat162 lo2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+                phi[j >> 1] = *reinterpret_cast<const uint32_t *>(&hi2);
+                plo[j >> 1] = *reinterpret_cast<const uint32_t *>(&lo2);
+            }
+            l += sum + __shfl_xor_sync(0xffffffffu, sum, 16);
+            mbar_wait(&S.pfree[st], ph ^ 1u, A.status);   // PV of chunk i-2 is done with the buffer
+            {
+                uint8_t *pr = sP + st * 2 * kPBytes + hl * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int cch = (upper ? 4 : 0) + c;
+                    const uint32_t sw = static_cast<uint32_t>((cch ^ (hl & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(pr + sw) =
+                        make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
+                    *reinterpret_cast<uint4 *>(pr + kPBytes + sw) =
+                        make_uint4(plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&S.pfull[st]);
+        }
+        // ---- epilogue: O^T column h / l_h (one split) or the raw partial
+        if (!upper) {
+            S.mh[hl] = m_ref;
+            S.lh[hl] = l;
+            float f = 1.f;
+            if (A.splits == 1) {
+                float z = l;
+                if (A.sinks && hv && m_ref != -INFINITY) z += exp2f(A.sinks[h0 + hl] * kLog2e - m_ref);
+                f = (z > 0.f && l > 0.f) ? 1.f / z : 0.f;
+            }
+            S.fin[hl] = f;
+        }
+        if (nch > 0) mbar_wait(&S.odone, 0, A.status);
+        named_bar_sync(kBarSm, kSmThreads);
+        tc_fence_after();
+        const int64_t obase = A.splits == 1
+                                  ? (static_cast<int64_t>(t) * H + h0) * kHD
+                                  : ((static_cast<int64_t>(t) * A.splits + split) * H + h0) * kHD;
+        float *dst = A.splits == 1 ? A.out : A.part_o;
+        const int hmax = min(kHG, H - h0);
+        // one output column per lane: every warp store is 128 contiguous bytes
+        if (nch == 0) {
+            for (int e = st_t; e < hmax * kHD; e += kSmThreads) dst[obase + e] = 0.f;
+        } else {
+#pragma unroll 1
+            for (int dt = 0; dt < 4; ++dt) {
+                const int d = dt * 128 + q * 32 + lane;
+                uint32_t r[4][16];
+#pragma unroll
+                for (int hb = 0; hb < 4; ++hb) tmem_ld16_raw(tmem + lane_off + kOCol + dt * kHG + hb * 16, r[hb]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int hb = 0; hb < 4; ++hb)
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int h = hb * 16 + c;
+                        if (h < hmax) dst[obase + h * kHD + d] = __uint_as_float(r[hb][c]) * S.fin[h];
+                    }
+            }
+        }
+        if (A.splits > 1 && !upper && hv) {
+            const int64_t mb = ((static_cast<int64_t>(t) * A.splits + split) * H + h0 + hl) * 2;
+            A.part_ml[mb + 0] = nch > 0 ? m_ref : -INFINITY;
+            A.part_ml[mb + 1] = nch > 0 ? l : 0.f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// out[t,h,:] = sum_s 2^(m_s - M) O_s / (sum_s 2^(m_s - M) l_s [+ 2^(sink log2e - M)]),
+// splits without rows (m = -inf) skipped.  CTA = (head, token); thread
+// (sub, c4) holds columns 4 c4 .. 4 c4 + 3 of splits sub, sub + nsub, ...
+// (at most kCombPer each, all loads in flight at once), and the nsub partial
+// sums meet in shared memory in a fixed order.
+constexpr int kCombPer = 8;
+
+__global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int h = blockIdx.x, t = blockIdx.y;
+    const int nsub = static_cast<int>(blockDim.x >> 7);
+    const int c4 = threadIdx.x & 127, sub = threadIdx.x >> 7;
+    __shared__ float wgt[64];
+    __shared__ float inv_z;
+    __shared__ float4 red[7][128];
+    const int ns = A.splits;
+    const float *mlb = A.part_ml + (static_cast<int64_t>(t) * ns * A.H + h) * 2;
+    const int64_t mstride = static_cast<int64_t>(A.H) * 2;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+        if (lane < ns) {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(mlb + lane * mstride));
+            m0 = x.x;
+            l0 = x.y;
+        }
+        if (lane + 32 < ns) {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(mlb + (lane + 32) * mstride));
+            m1 = x.x;
+            l1 = x.y;
+        }
+        float M = fmaxf(m0, m1);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float sink = A.sinks ? A.sinks[h] * kLog2e : -INFINITY;
+        const float Mall = fmaxf(M, sink);
+        const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - Mall);
+        const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - Mall);
+        if (lane < ns) wgt[lane] = w0;
+        if (lane + 32 < ns) wgt[lane + 32] = w1;
+        float z = w0 * l0 + w1 * l1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        if (lane == 0) {
+            const bool any = M != -INFINITY;
+            if (A.sinks && any) z += exp2f(sink - Mall);
+            inv_z = (any && z > 0.f) ? 1.f / z : 0.f;
+        }
+    }
+    __syncthreads();
+    const float *pb = A.part_o + (static_cast<int64_t>(t) * ns * A.H + h) * kHD + 4 * c4;
+    const int64_t pstride = static_cast<int64_t>(A.H) * kHD;
+    float4 v[kCombPer];
+#pragma unroll
+    for (int k = 0; k < kCombPer; ++k) {
+        const int sp = sub + k * nsub;
+        if (sp < ns && wgt[sp] != 0.f) v[k] = __ldcg(reinterpret_cast<const float4 *>(pb + sp * pstride));
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kCombPer; ++k) {
+        const int sp = sub + k * nsub;
+        if (sp < ns && wgt[sp] != 0.f) {
+            const float w = wgt[sp];
+            acc.x += w * v[k].x;
+            acc.y += w * v[k].y;
+            acc.z += w * v[k].z;
+            acc.w += w * v[k].w;
+        }
+    }
+    if (sub > 0) red[sub - 1][c4] = acc;
+    __syncthreads();
+    if (sub == 0) {
+        for (int j = 0; j + 1 < nsub; ++j) {
+            const float4 r = red[j][c4];
+            acc.x += r.x;
+            acc.y += r.y;
+            acc.z += r.z;
+            acc.w += r.w;
+        }
+        const float iz = inv_z;
+        float *o = A.out + (static_cast<int64_t>(t) * A.H + h) * kHD + 4 * c4;
+        *reinterpret_cast<float4 *>(o) = make_float4(acc.x * iz, acc.y * iz, acc.z * iz, acc.w * iz);
+    }
+}
+
+}  // namespace
+
+size_t attention_tc_smem_bytes() { return 1024 + kQBytes + 2 * kRowsBytes + 4 * kPBytes + sizeof(TcSmem); }
+
+cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t T,
+                                const csa_params_t &p, const WsPlan &plan, const void *q,
+                                const float *sinks, float *out, float *part_o, float *part_ml,
+                                int32_t *status, bool early_q) {
+    if (T <= 0) return cudaSuccess;
+    CUtensorMap tq;
+    const int H = p.n_heads;
+    if (encode_tensor_map_2d_bf16(&tq, q, kHD, static_cast<uint64_t>(T) * H, kHD * 2, 64, kHG) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    TcParams A;
+    A.R = src;
+    A.H = H;
+    A.splits = plan.splits;
+    A.rows_split = plan.rows_split;
+    A.scale_log2 = p.scale * kLog2e;
+    A.sinks = sinks;
+    A.out = out;
+    A.part_o = part_o;
+    A.part_ml = part_ml;
+    A.status = status;
+    A.early_q = early_q ? 1 : 0;
+    const size_t smem = attention_tc_smem_bytes();
+    cudaError_t e = set_kernel_smem(attention_tc_kernel, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(plan.splits, (H + kHG - 1) / kHG, T);
+    e = launch_pdl(attention_tc_kernel, grid, dim3(kTcThreads), smem, lc.stream, tq, A);
+    if (e != cudaSuccess || plan.splits == 1) return e;
+    e = set_kernel_smem(combine_tc_kernel, 0);
+    if (e != cudaSuccess) return e;
+    // splits <= 64 (the plan's cap), so nsub <= 8 and blockDim <= 1024
+    const int nsub = (plan.splits + kCombPer - 1) / kCombPer;
+    return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub), 0, lc.stream, A);
+}
+
+}  // namespace csa

@@ -15,8 +15,10 @@ namespace csa {
 
 // Device-independent grid targets (sized for ~150-SM parts).
 constexpr int kTargetCtas = 296;
-constexpr int kAttnChunk = 32;   // rows per attention chunk (one online-softmax step)
-constexpr int kHeadGroup = 16;   // query heads per attention CTA
+constexpr int kTcChunk = 64;     // rows per chunk of the tensor-core attention
+constexpr int kTcHeads = 64;     // heads per tensor-core attention CTA
+constexpr int kAttnCtas = 148;   // attention CTAs to aim for (about one per SM)
+constexpr int kHeadGroup = 16;   // n_heads must be a multiple of this
 constexpr int kMaxFilterChunk = 4096;  // scores per top-k filter CTA (multi-CTA mode)
 constexpr int kMaxPerTok = 512;        // top-k filter CTAs per token
 
@@ -37,9 +39,7 @@ struct WsPlan {
     int32_t topk_chunk = 0;  // scores per top-k filter CTA
     int32_t topk_per_tok = 1;  // top-k filter CTAs per token (1: one CTA owns the row)
     int32_t splits = 1;      // attention splits per token
-    int32_t rows_split = 0;  // rows per attention split (multiple of kAttnChunk)
-    int32_t attn_cluster = 1;  // attention CTAs per thread-block cluster along the splits
-                               // (divides splits): they merge their partials on chip
+    int32_t rows_split = 0;  // rows per attention split (multiple of kTcChunk)
     // Layout: [per-token state | ... free ... | data].  The state slots sit at
     // the front at offsets that depend only on the token index; the data
     // regions are packed against the end of the caller's workspace, so no
@@ -140,10 +140,13 @@ cudaError_t launch_topk(const Launch &lc, const csa_layout_t &L, const csa_param
 cudaError_t launch_gather(const Launch &lc, const RowSource &src, int32_t T, void *kv_buf,
                           int32_t *kv_len, int32_t *status);
 
-cudaError_t launch_attention(const Launch &lc, const RowSource &src, int32_t T,
-                             const csa_params_t &p, const WsPlan &plan, const void *q,
-                             const float *sinks, float *out, float *part_o, float *part_ml,
-                             int32_t *status, bool early_q = false);
+// Shared-KV attention on the tensor cores (csa_attention_tc.cu): grid
+// (splits, ceil(H / 64), T), partials merged by a combine kernel when a
+// token has several splits.
+cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t T,
+                                const csa_params_t &p, const WsPlan &plan, const void *q,
+                                const float *sinks, float *out, float *part_o, float *part_ml,
+                                int32_t *status, bool early_q = false);
 
 // Launch helper: programmatic dependent launch on, so each kernel's prologue
 // may overlap the previous kernel's tail (kernels wait with griddepcontrol).
@@ -160,28 +163,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
-// Programmatic dependent launch of a grid in clusters of cluster_x CTAs
-// along x (cluster_x == 1: a plain launch_pdl).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                               cudaStream_t stream, int cluster_x, Args &&...args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = cluster_x > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
