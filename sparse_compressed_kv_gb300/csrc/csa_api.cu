@@ -23,7 +23,7 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     topk_grid(T, max_comp_rows, &w.topk_chunk, &w.topk_per_tok);
     // Attention: a token's row slots (the window starts at a multiple of 4)
     // in chunks of kTcChunk; splits per token so that about one CTA per SM
-    // runs, at most 64 (the combine's limit), each a whole number of chunks.
+    // runs, at most 128 (the combine's limit), each a whole number of chunks.
     const int64_t rows_max =
         rows_max_in >= 0 ? rows_max_in : static_cast<int64_t>(p.top_k) + p.window;
     const int64_t comp_max = rows_max > p.window ? rows_max - p.window : 0;
@@ -32,7 +32,7 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     const int64_t groups = (p.n_heads + kTcHeads - 1) / kTcHeads;
     int64_t splits = kAttnCtas / ((T > 0 ? T : 1) * groups);
     if (splits > chunks) splits = chunks;
-    if (splits > 64) splits = 64;
+    if (splits > 128) splits = 128;
     if (splits < 1) splits = 1;
     const int64_t per = (chunks + splits - 1) / splits;
     w.rows_split = static_cast<int32_t>(per * kTcChunk);

@@ -55,7 +55,8 @@ constexpr int kSmThreads = 128;                // warps 2..5
 constexpr int kBarSm = 1;                      // named barrier of the softmax warps
 constexpr int kLdThreads = 32 * kLdWarps;
 constexpr int kHG = 64;                        // heads per CTA (MMA M of QK^T)
-constexpr int kChunk = 64;                     // rows per chunk (QK^T N, PV K)
+constexpr int kChunk = kTcChunk;               // rows per chunk (QK^T N, PV K): 64
+static_assert(kChunk == 64, "the softmax gives each lane 32 rows of a chunk");
 constexpr int kQBytes = 8 * kHG * 128;         // 64 KiB: Q, eight 64-column boxes
 constexpr int kRowBox = kChunk * 128;          // 8 KiB: 64 columns of a chunk's rows
 constexpr int kRowsBytes = 8 * kRowBox;        // 64 KiB per stage
@@ -560,10 +561,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // out[t,h,:] = sum_s 2^(m_s - M) O_s / (sum_s 2^(m_s - M) l_s [+ 2^(sink log2e - M)]),
 // splits without rows (m = -inf) skipped.  CTA = (head, token); thread
-// (sub, c4) holds columns 4 c4 .. 4 c4 + 3 of splits sub, sub + nsub, ...
-// (at most kCombPer each, all loads in flight at once), and the nsub partial
+// (sub, c4) holds columns 4 c4 .. 4 c4 + 3 of splits sub, sub + nsub, ...,
+// loaded kCombPer at a time (all of them in flight), and the nsub partial
 // sums meet in shared memory in a fixed order.
 constexpr int kCombPer = 8;
+constexpr int kMaxSplits = 128;
 
 __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
     pdl_wait();
@@ -571,7 +573,7 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
     const int h = blockIdx.x, t = blockIdx.y;
     const int nsub = static_cast<int>(blockDim.x >> 7);
     const int c4 = threadIdx.x & 127, sub = threadIdx.x >> 7;
-    __shared__ float wgt[64];
+    __shared__ float wgt[kMaxSplits];
     __shared__ float inv_z;
     __shared__ float4 red[7][128];
     const int ns = A.splits;
@@ -579,27 +581,29 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
     const int64_t mstride = static_cast<int64_t>(A.H) * 2;
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-        if (lane < ns) {
-            const float2 x = __ldcg(reinterpret_cast<const float2 *>(mlb + lane * mstride));
-            m0 = x.x;
-            l0 = x.y;
+        float m[4], lv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[k] = -INFINITY;
+            lv[k] = 0.f;
+            if (lane + 32 * k < ns) {
+                const float2 x = __ldcg(reinterpret_cast<const float2 *>(mlb + (lane + 32 * k) * mstride));
+                m[k] = x.x;
+                lv[k] = x.y;
+            }
         }
-        if (lane + 32 < ns) {
-            const float2 x = __ldcg(reinterpret_cast<const float2 *>(mlb + (lane + 32) * mstride));
-            m1 = x.x;
-            l1 = x.y;
-        }
-        float M = fmaxf(m0, m1);
+        float M = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         const float sink = A.sinks ? A.sinks[h] * kLog2e : -INFINITY;
         const float Mall = fmaxf(M, sink);
-        const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - Mall);
-        const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - Mall);
-        if (lane < ns) wgt[lane] = w0;
-        if (lane + 32 < ns) wgt[lane + 32] = w1;
-        float z = w0 * l0 + w1 * l1;
+        float z = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float w = m[k] == -INFINITY ? 0.f : exp2f(m[k] - Mall);
+            if (lane + 32 * k < ns) wgt[lane + 32 * k] = w;
+            z += w * lv[k];
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         if (lane == 0) {
@@ -611,22 +615,24 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
     __syncthreads();
     const float *pb = A.part_o + (static_cast<int64_t>(t) * ns * A.H + h) * kHD + 4 * c4;
     const int64_t pstride = static_cast<int64_t>(A.H) * kHD;
-    float4 v[kCombPer];
-#pragma unroll
-    for (int k = 0; k < kCombPer; ++k) {
-        const int sp = sub + k * nsub;
-        if (sp < ns && wgt[sp] != 0.f) v[k] = __ldcg(reinterpret_cast<const float4 *>(pb + sp * pstride));
-    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = sub; base < ns; base += kCombPer * nsub) {
+        float4 v[kCombPer];
 #pragma unroll
-    for (int k = 0; k < kCombPer; ++k) {
-        const int sp = sub + k * nsub;
-        if (sp < ns && wgt[sp] != 0.f) {
-            const float w = wgt[sp];
-            acc.x += w * v[k].x;
-            acc.y += w * v[k].y;
-            acc.z += w * v[k].z;
-            acc.w += w * v[k].w;
+        for (int k = 0; k < kCombPer; ++k) {
+            const int sp = base + k * nsub;
+            if (sp < ns && wgt[sp] != 0.f) v[k] = __ldcg(reinterpret_cast<const float4 *>(pb + sp * pstride));
+        }
+#pragma unroll
+        for (int k = 0; k < kCombPer; ++k) {
+            const int sp = base + k * nsub;
+            if (sp < ns && wgt[sp] != 0.f) {
+                const float w = wgt[sp];
+                acc.x += w * v[k].x;
+                acc.y += w * v[k].y;
+                acc.z += w * v[k].z;
+                acc.w += w * v[k].w;
+            }
         }
     }
     if (sub > 0) red[sub - 1][c4] = acc;
@@ -679,8 +685,10 @@ cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t 
     if (e != cudaSuccess || plan.splits == 1) return e;
     e = set_kernel_smem(combine_tc_kernel, 0);
     if (e != cudaSuccess) return e;
-    // splits <= 64 (the plan's cap), so nsub <= 8 and blockDim <= 1024
-    const int nsub = (plan.splits + kCombPer - 1) / kCombPer;
+    // splits <= kMaxSplits (the plan's cap): nsub <= 8, blockDim <= 1024
+    if (plan.splits > kMaxSplits) return cudaErrorInvalidValue;
+    int nsub = (plan.splits + kCombPer - 1) / kCombPer;
+    nsub = nsub < 8 ? nsub : 8;
     return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub), 0, lc.stream, A);
 }
 
