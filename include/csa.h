@@ -71,7 +71,9 @@ typedef enum {
 #define CSA_DEV_BAD_LAYOUT  0x04  /* tok_seq outside [0,B), tok_pos < 0, bad comp_off */
 #define CSA_DEV_CAPACITY    0x08  /* a sequence holds more blocks than max_comp_rows */
 #define CSA_DEV_BAD_LENGTH  0x10  /* kv_len outside [0, top_k + window] */
-#define CSA_DEV_TIMEOUT     0x20  /* reserved for bounded waits */
+#define CSA_DEV_TIMEOUT     0x20  /* a bounded wait inside a kernel gave up */
+#define CSA_DEV_CHECK       0x40  /* libcsa_checks.so only: an index inside the library
+                                     left its array; the access was skipped */
 
 /* Where each query token's rows live.  Device arrays unless marked (host). */
 typedef struct {

@@ -15,7 +15,10 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libcsa.so")
+# CSA_CHECKS=1 in the environment selects the build with internal bounds
+# checks (libcsa_checks.so: same entry points, CSA_DEV_CHECK on a failed check)
+LIB_PATH = os.path.join(_HERE, "libcsa_checks.so" if os.environ.get("CSA_CHECKS") == "1"
+                        else "libcsa.so")
 
 CSA_OK = 0
 STATUS_NAMES = {
@@ -24,6 +27,7 @@ STATUS_NAMES = {
 }
 DEV_BAD_INDEX, DEV_MISSING_SWA, DEV_BAD_LAYOUT = 0x01, 0x02, 0x04
 DEV_CAPACITY, DEV_BAD_LENGTH, DEV_TIMEOUT = 0x08, 0x10, 0x20
+DEV_CHECK = 0x40
 
 EXPORTS = ("csa_status_string", "csa_abi_version", "csa_workspace_size", "csa_indexer_scores",
            "csa_topk", "csa_indexer_topk", "csa_gather_mixed", "csa_sparse_mqa_decode", "csa_decode",
@@ -60,13 +64,14 @@ _lib = None
 
 
 def load() -> ctypes.CDLL:
-    """Load libcsa.so (built by sparse_compressed_kv_gb300.build); raise if absent."""
+    """Load libcsa.so, or libcsa_checks.so under CSA_CHECKS=1 (built by
+    sparse_compressed_kv_gb300.build); raise if absent."""
     global _lib
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"libcsa.so not found at {LIB_PATH}: run the build "
-                           "(python -m sparse_compressed_kv_gb300.build) first")
+        raise RuntimeError(f"{os.path.basename(LIB_PATH)} not found at {LIB_PATH}: run the "
+                           "build (python -m sparse_compressed_kv_gb300.build --all) first")
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.c_void_p
     L = ctypes.POINTER(csa_layout_t)

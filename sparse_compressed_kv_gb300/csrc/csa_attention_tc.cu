@@ -345,7 +345,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                              ? j
                                              : A.R.idx[static_cast<int64_t>(t) * A.R.top_k + j];
                     if (sidx < 0 || sidx >= k.n_vis) bad |= CSA_DEV_BAD_INDEX;
-                    else src = static_cast<const __nv_bfloat16 *>(A.R.comp_kv) + (k.off + sidx) * kHD;
+                    else if (CSA_CHECK(k.off + sidx < A.R.L.total_comp_rows, A.status))
+                        src = static_cast<const __nv_bfloat16 *>(A.R.comp_kv) + (k.off + sidx) * kHD;
                 } else if (j >= k.wslot) {
                     const int64_t x = k.first + (j - k.wslot);
                     if (x < k.first_res) bad |= CSA_DEV_MISSING_SWA;
@@ -571,6 +572,7 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
     pdl_wait();
     pdl_launch_dependents();
     const int h = blockIdx.x, t = blockIdx.y;
+    if (!CSA_CHECK(A.splits <= kMaxSplits, A.status)) return;
     const int nsub = static_cast<int>(blockDim.x >> 7);
     const int c4 = threadIdx.x & 127, sub = threadIdx.x >> 7;
     __shared__ float wgt[kMaxSplits];

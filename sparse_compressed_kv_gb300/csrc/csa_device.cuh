@@ -105,6 +105,21 @@ __device__ __forceinline__ void raise_status(int32_t *st, int bits) {
     if (bits && st) atomicOr(st, bits);
 }
 
+// Bounds checks of the build with CSA_CHECKS defined (libcsa_checks.so): an
+// index inside the library that leaves its array sets CSA_DEV_CHECK in the
+// status word and the access is skipped, never trapped.  In the default build
+// the condition is not evaluated: every such index is in range by
+// construction (the layout and argument checks come first).
+#ifdef CSA_CHECKS
+__device__ __forceinline__ bool csa_check(bool ok, int32_t *st) {
+    if (!ok) raise_status(st, CSA_DEV_CHECK);
+    return ok;
+}
+#define CSA_CHECK(cond, st) ::csa::csa_check((cond), (st))
+#else
+#define CSA_CHECK(cond, st) true
+#endif
+
 // Order-preserving map of an f32 score to u32 (larger score -> larger key);
 // -0.0 is folded onto +0.0 so the two tie.
 __device__ __forceinline__ uint32_t score_key(float f) {

@@ -283,7 +283,8 @@ __device__ __forceinline__ void finalize_segment(const DecParams &P, DecSmem &S,
     for (int j = 0; j < PER; ++j)
         if (hv[j] && static_cast<uint32_t>(hb + j) >= d1) atomicAdd(gh + hb + j, hv[j]);
     // every entry with digit >= d1, in block order, to the slot
-    const int slot = S.sb[tk] + (c - cta_of(S.U[tk], K32, Ge));
+    int slot = S.sb[tk] + (c - cta_of(S.U[tk], K32, Ge));
+    if (!CSA_CHECK(slot >= 0 && slot < P.f.slots, P.status)) slot = 0;   // (checked builds only)
     uint64_t *dst = P.f.cand + static_cast<int64_t>(slot) * P.f.cap;
     const int R = odd_run(static_cast<int>(len), NT);
     const int r0 = min(static_cast<int>(len), gt * R);
@@ -320,7 +321,9 @@ __device__ __forceinline__ void finalize_segment(const DecParams &P, DecSmem &S,
         uint32_t *tkt = &reinterpret_cast<TokCounters *>(P.f.state + static_cast<int64_t>(tk) * kStateWords +
                                                          kD1Bins + kD2Bins)->ticket;
         asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(tkt) : "memory");
-        if (prev + 1 == static_cast<uint32_t>(S.sb[tk + 1] - S.sb[tk])) S.resolve[S.nresolve++] = tk;
+        if (prev + 1 == static_cast<uint32_t>(S.sb[tk + 1] - S.sb[tk]) &&
+            CSA_CHECK(S.nresolve < kDecMaxTokens, P.status))
+            S.resolve[S.nresolve++] = tk;
     }
 }
 
@@ -389,7 +392,8 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
         group_find_digit<kWarps, 8>(v, hb, kk, S.bt, warp, 0, S);
         mbar_wait(&S.rbar, ph, P.status);
         // an odd slot's copy brought one stale entry past its end
-        if (tid < nseg && (m.x & 1u)) stage[soff + m.x] = kNoEntry;
+        if (tid < nseg && (m.x & 1u) && CSA_CHECK(soff + m.x < kStageEntries, P.status))
+            stage[soff + m.x] = kNoEntry;
         if (tid == 0) S.rphase = ph ^ 1u;
         __syncthreads();
         from_row = S.fd < 0;   // fewer than k keys >= the bound: it proves nothing
@@ -776,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         part[c4] = fmaf(__ldg(wt + c4 * 16 + i), fmaxf(v[c4][i], 0.f), part[c4]);
             }
             const float score = (part[0] + part[1]) + (part[2] + part[3]);
-            if (valid) P.scores[static_cast<int64_t>(tk) * P.ld + s] = score;
+            if (valid && CSA_CHECK(s < P.ld, P.status)) P.scores[static_cast<int64_t>(tk) * P.ld + s] = score;
             if (kFused) {
                 const uint32_t key = score_key(score);
                 const int64_t lo = (tl.u - ua) * kBoxRows + row;

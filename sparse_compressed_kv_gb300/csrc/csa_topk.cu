@@ -344,7 +344,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                         const uint32_t j = j0 + tid;
                         if (j < c) v0 = S.stage[w * kPerWarpCap + j];
                         __syncthreads();
-                        if (j < c) S.stage[S.prefix[w] + j] = v0;
+                        if (j < c && CSA_CHECK(S.prefix[w] + j < kStageCap, P.status))
+                            S.stage[S.prefix[w] + j] = v0;
                         __syncthreads();
                     }
                 }
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
             for (int q = 0; q < kMaxPerThread; ++q) {
                 const bool keep = q * 32 < span && wbase + q * 32 < b1 && (keys[q] >> kD1Shift) >= d1;
                 const unsigned m = __ballot_sync(0xffffffffu, keep);
-                if (keep)
+                if (keep && CSA_CHECK(pos + __popc(m & lt) < static_cast<uint32_t>(P.chunk), P.status))
                     slot[pos + __popc(m & lt)] = (static_cast<uint64_t>(keys[q]) << 32) |
                                                  static_cast<uint32_t>(wbase + q * 32);
                 pos += __popc(m);
@@ -492,6 +493,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                     if (sl < pt) {
                         const uint32_t cnt = S.prefix[sl + 1] - S.prefix[sl];
                         uint64_t *dst = S.stage + S.prefix[sl];
+                        if (!CSA_CHECK(S.prefix[sl] + cnt <= static_cast<uint32_t>(kStageCap), P.status))
+                            continue;
                         if (se0 < cnt) {
                             dst[se0] = sv[u].x;
                             if (gathered) collect(sv[u].x);
@@ -517,6 +520,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectPara
                     const uint32_t e0 = sp + (g - S.gprefix[lo]) * 8;
                     const uint64_t *src = base + static_cast<int64_t>(lo) * P.chunk + e0;
                     uint64_t *dst = S.stage + S.prefix[lo] + e0;
+                    if (!CSA_CHECK(S.prefix[lo] + cnt <= static_cast<uint32_t>(kStageCap), P.status))
+                        continue;
                     uint64_t val[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) val[u] = e0 + u < cnt ? __ldcg(src + u) : 0ull;

@@ -37,6 +37,17 @@ def test_library_exports_every_declared_symbol(lib):
     assert csa.abi_version() == 1
 
 
+def test_checked_build_exports_the_same_symbols():
+    # libcsa_checks.so: the same sources with CSA_CHECKS defined (internal
+    # bounds checks report CSA_DEV_CHECK); loaded on its own, not through csa
+    path = B.build(checks=True)
+    chk = ctypes.CDLL(path)
+    for fn in declared_functions():
+        assert hasattr(chk, fn), fn
+    chk.csa_abi_version.restype = ctypes.c_int
+    assert chk.csa_abi_version() == 1
+
+
 def test_status_strings(lib):
     assert csa.status_string(0) == "CSA_OK"
     assert csa.status_string(7) == "CSA_ERR_WORKSPACE"
