@@ -231,6 +231,75 @@ csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *para
                             const void *comp_kv, const void *q, const float *sinks, float *out,
                             int32_t *dev_status, void *ws, size_t ws_bytes, void *stream);
 
+/* Sharded single-sequence decode ([Audit 1M], PART 2, "Total KV cache @ 1M
+ * context": the KV cache sharded across GPUs).  One sequence (num_seqs == 1,
+ * else CSA_ERR_UNSUPPORTED) whose compressed blocks are cut into contiguous
+ * ranges: shard g holds blocks [lo_g, hi_g) as rows 0 .. hi_g - lo_g - 1 of
+ * its own k_idx and comp_kv (the same row formats as above).  `layout` is the
+ * whole sequence's layout as every other call takes it (comp_off = {0,
+ * n_comp}); a shard's own caches replace k_idx / comp_kv.  One step:
+ *   1. each shard: csa_shard_candidates -> its k' = min(top_k, its visible
+ *      blocks) best blocks, global block indices and the scores they won on;
+ *   2. exchange the candidates (all-gather), then csa_shard_merge on any
+ *      device: the global top-k by (score descending, block index ascending),
+ *      identical to csa_topk on the whole score row, because a block of the
+ *      global top-k is among its own shard's k best;
+ *   3. each shard: csa_shard_attention over its own selected rows, and one
+ *      device csa_window_attention over the window rows: unnormalised
+ *      partials (O scaled to m, m in log2 units, l), no sink;
+ *   4. exchange the partials, then csa_shard_combine: the log-sum-exp merge,
+ *      the sink (if any) in the denominator.
+ * No call communicates: the exchanges are the caller's (NCCL all-gathers,
+ * or plain copies on one device).  Buffers are device memory, caller-owned.
+ *
+ * csa_shard_workspace_size: bytes of workspace for the shard calls with this
+ * range (zeroed once before first use, as for csa_decode).
+ * csa_shard_candidates: cand_score f32 [T, top_k], cand_idx int32 [T, top_k]
+ * (global indices, -1 past n_cand[t]), n_cand int32 [T].
+ * csa_shard_merge: shard_bounds (host) int64 [G + 1], G <= 8, lo_0 <= ... <=
+ * hi_{G-1}; cand_* [G][T][top_k] and n_cand [G][T] as gathered; writes idx
+ * int32 [T, top_k] (global, ascending, -1 padded), n_sel [T], shard_idx int32
+ * [G][T][top_k] (each shard's part of idx in its own rows, ascending) and
+ * shard_nsel [G][T].  A candidate index outside [0, hi_{G-1}) sets
+ * CSA_DEV_BAD_INDEX and is dropped; a count outside [0, top_k] sets
+ * CSA_DEV_BAD_LENGTH and is clamped.  G * top_k <= 16384.
+ * csa_shard_attention: shard_idx / shard_nsel as the merge gave them for
+ * this shard ([T][top_k], [T]); part_o f32 [T, H, 512], part_ml f32 [T, H, 2].
+ * csa_window_attention: the window rows of every token (from the layout's
+ * ring), as a partial of the same form.
+ * csa_shard_combine: num_parts partials laid out [P][T][H][512] and
+ * [P][T][H][2] (P <= 128) -> out f32 [T, H, 512]; a partial with m = -inf
+ * carries no rows. */
+csa_status_t csa_shard_workspace_size(const csa_layout_t *layout, const csa_params_t *params,
+                                      int64_t shard_lo, int64_t shard_hi,
+                                      size_t *bytes /* (host) out */);
+
+csa_status_t csa_shard_candidates(const csa_layout_t *layout, const csa_params_t *params,
+                                  int64_t shard_lo, int64_t shard_hi, const void *q_idx,
+                                  const float *w_idx, const void *k_idx_shard, float *cand_score,
+                                  int32_t *cand_idx, int32_t *n_cand, int32_t *dev_status, void *ws,
+                                  size_t ws_bytes, void *stream);
+
+csa_status_t csa_shard_merge(int32_t num_tokens, int32_t top_k, int32_t num_shards,
+                             const int64_t *shard_bounds /* (host) */, const float *cand_score,
+                             const int32_t *cand_idx, const int32_t *n_cand, int32_t *idx,
+                             int32_t *n_sel, int32_t *shard_idx, int32_t *shard_nsel,
+                             int32_t *dev_status, void *stream);
+
+csa_status_t csa_shard_attention(const csa_layout_t *layout, const csa_params_t *params,
+                                 int64_t shard_lo, int64_t shard_hi, const int32_t *shard_idx,
+                                 const int32_t *shard_nsel, const void *comp_kv_shard,
+                                 const void *q, float *part_o, float *part_ml, int32_t *dev_status,
+                                 void *ws, size_t ws_bytes, void *stream);
+
+csa_status_t csa_window_attention(const csa_layout_t *layout, const csa_params_t *params,
+                                  const void *q, float *part_o, float *part_ml,
+                                  int32_t *dev_status, void *ws, size_t ws_bytes, void *stream);
+
+csa_status_t csa_shard_combine(int32_t num_parts, int32_t num_tokens, int32_t n_heads,
+                               const float *part_o, const float *part_ml, const float *sinks,
+                               float *out, int32_t *dev_status, void *stream);
+
 /* FP4 indexer key cache ([Audit rewrite], C4, and [Audit 1M], M1: the
  * indexer keys are cached in FP4, the paper's section 5.2.1).  The pages fix
  * no format; this library reads it as OCP MXFP4: e2m1 elements (0, 0.5, 1,

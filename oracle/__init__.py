@@ -338,6 +338,50 @@ def attention(*args, **kwargs):
     return default().attention(*args, **kwargs)
 
 
+def _bf16_array(bits) -> np.ndarray:
+    """bf16 bit patterns -> float64 (exact: a bf16 value is the top half of an f32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def attention_partial(q, rows, scale):
+    """Unnormalised attention of one part of a token's rows ([Audit 1M] D5:
+    every row is the key and the value of all heads), for the sharded step's
+    log-sum-exp merge.  q [H, hd] and rows [n, hd] as uint16 bf16 bits.
+    Returns (O [H, hd], m [H], l [H]) in float64, natural-log units:
+    m_h = max_j z_hj, l_h = sum_j exp(z_hj - m_h), O_h = sum_j exp(z_hj - m_h) row_j,
+    z_hj = scale * q_h . row_j; an empty part gives (0, -inf, 0)."""
+    qf = _bf16_array(q)
+    rf = _bf16_array(rows).reshape(-1, qf.shape[1])
+    H, hd = qf.shape
+    if rf.shape[0] == 0:
+        return np.zeros((H, hd)), np.full(H, -np.inf), np.zeros(H)
+    z = scale * (qf @ rf.T)                      # [H, n]
+    m = z.max(axis=1)
+    e = np.exp(z - m[:, None])
+    return e @ rf, m, e.sum(axis=1)
+
+
+def combine_partials(O, m, l, sinks=None):
+    """out [H, hd] = sum_p exp(m_p - M) O_p / (sum_p exp(m_p - M) l_p [+ exp(sink_h - M)]),
+    M = max_p m_p, over parts p (arrays O [P, H, hd], m [P, H], l [P, H]);
+    parts with m = -inf carry nothing.  Same merge as the sink identity of
+    [Audit 1M] D6: the sink is one more logit with a zero value row."""
+    O = np.asarray(O, dtype=np.float64)
+    m = np.asarray(m, dtype=np.float64)
+    l = np.asarray(l, dtype=np.float64)
+    M = m.max(axis=0)                            # [H]
+    if sinks is not None:
+        M = np.maximum(M, np.asarray(sinks, dtype=np.float64))
+    w = np.where(np.isfinite(m), np.exp(m - np.where(np.isfinite(M), M, 0.0)), 0.0)   # [P, H]
+    num = (w[:, :, None] * O).sum(axis=0)
+    den = (w * l).sum(axis=0)
+    if sinks is not None:
+        den = den + np.exp(np.asarray(sinks, dtype=np.float64) - M)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        return np.where(den[:, None] > 0, num / den[:, None], 0.0)
+
+
 def decode(*args, **kwargs):
     return default().decode(*args, **kwargs)
 

@@ -32,7 +32,10 @@ DEV_CHECK = 0x40
 EXPORTS = ("csa_status_string", "csa_abi_version", "csa_workspace_size", "csa_indexer_scores",
            "csa_topk", "csa_indexer_topk", "csa_gather_mixed", "csa_sparse_mqa_decode", "csa_decode",
            "csa_hca_workspace_size", "csa_hca_decode", "csa_fp4_quantize_keys",
-           "csa_indexer_scores_fp4", "csa_decode_fp4")
+           "csa_indexer_scores_fp4", "csa_decode_fp4", "csa_shard_workspace_size",
+           "csa_shard_candidates", "csa_shard_merge", "csa_shard_attention", "csa_window_attention",
+           "csa_shard_combine")
+MAX_SHARDS = 8  # csa_shard_merge's limit (include/csa.h)
 FP4_ROW = 80  # bytes per MXFP4 key row (include/csa.h)
 
 
@@ -92,6 +95,12 @@ def load() -> ctypes.CDLL:
     lib.csa_fp4_quantize_keys.argtypes = [i64, P, P, P]
     lib.csa_indexer_scores_fp4.argtypes = [L, Pm, P, P, P, P, i64, P, P]
     lib.csa_decode_fp4.argtypes = [L, Pm, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.csa_shard_workspace_size.argtypes = [L, Pm, i64, i64, ctypes.POINTER(sz)]
+    lib.csa_shard_candidates.argtypes = [L, Pm, i64, i64, P, P, P, P, P, P, P, P, sz, P]
+    lib.csa_shard_merge.argtypes = [i32, i32, i32, ctypes.POINTER(i64), P, P, P, P, P, P, P, P, P]
+    lib.csa_shard_attention.argtypes = [L, Pm, i64, i64, P, P, P, P, P, P, P, P, sz, P]
+    lib.csa_window_attention.argtypes = [L, Pm, P, P, P, P, P, sz, P]
+    lib.csa_shard_combine.argtypes = [i32, i32, i32, P, P, P, P, P, P]
     for fn in EXPORTS[2:]:
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
@@ -260,3 +269,58 @@ def csa_decode_fp4(layout: Layout, prm: csa_params_t, q_idx, w_idx, k_fp4, comp_
         ctypes.byref(lc), ctypes.byref(prm), _p(q_idx), _p(w_idx), _p(k_fp4), _p(comp_kv), _p(q),
         _p(sinks), _p(out), _p(idx_out), _p(dev_status), _p(ws), int(ws.numel()),
         _stream(stream)))
+
+
+# ---------------------------------------------------------------- sharded decode
+
+def csa_shard_workspace_size(layout: Layout, prm: csa_params_t, lo: int, hi: int) -> int:
+    n = ctypes.c_size_t(0)
+    lc = layout.c()
+    _check("csa_shard_workspace_size", load().csa_shard_workspace_size(
+        ctypes.byref(lc), ctypes.byref(prm), int(lo), int(hi), ctypes.byref(n)))
+    return int(n.value)
+
+
+def csa_shard_candidates(layout: Layout, prm: csa_params_t, lo: int, hi: int, q_idx, w_idx,
+                         k_idx_shard, cand_score, cand_idx, n_cand, dev_status, ws, stream=None):
+    lc = layout.c()
+    _check("csa_shard_candidates", load().csa_shard_candidates(
+        ctypes.byref(lc), ctypes.byref(prm), int(lo), int(hi), _p(q_idx), _p(w_idx),
+        _p(k_idx_shard), _p(cand_score), _p(cand_idx), _p(n_cand), _p(dev_status), _p(ws),
+        int(ws.numel()), _stream(stream)))
+
+
+def csa_shard_merge(bounds, cand_score, cand_idx, n_cand, idx, n_sel, shard_idx, shard_nsel,
+                    dev_status, stream=None):
+    """cand_* [G, T, top_k], n_cand [G, T] -> idx [T, top_k], n_sel [T],
+    shard_idx [G, T, top_k], shard_nsel [G, T]; bounds: G + 1 ints (host)."""
+    G, T, K = (int(x) for x in cand_idx.shape)
+    b = (ctypes.c_int64 * (G + 1))(*[int(x) for x in bounds])
+    _check("csa_shard_merge", load().csa_shard_merge(
+        T, K, G, b, _p(cand_score), _p(cand_idx), _p(n_cand), _p(idx), _p(n_sel), _p(shard_idx),
+        _p(shard_nsel), _p(dev_status), _stream(stream)))
+
+
+def csa_shard_attention(layout: Layout, prm: csa_params_t, lo: int, hi: int, shard_idx,
+                        shard_nsel, comp_kv_shard, q, part_o, part_ml, dev_status, ws,
+                        stream=None):
+    lc = layout.c()
+    _check("csa_shard_attention", load().csa_shard_attention(
+        ctypes.byref(lc), ctypes.byref(prm), int(lo), int(hi), _p(shard_idx), _p(shard_nsel),
+        _p(comp_kv_shard), _p(q), _p(part_o), _p(part_ml), _p(dev_status), _p(ws),
+        int(ws.numel()), _stream(stream)))
+
+
+def csa_window_attention(layout: Layout, prm: csa_params_t, q, part_o, part_ml, dev_status, ws,
+                         stream=None):
+    lc = layout.c()
+    _check("csa_window_attention", load().csa_window_attention(
+        ctypes.byref(lc), ctypes.byref(prm), _p(q), _p(part_o), _p(part_ml), _p(dev_status),
+        _p(ws), int(ws.numel()), _stream(stream)))
+
+
+def csa_shard_combine(part_o, part_ml, out, dev_status, sinks=None, stream=None):
+    """part_o [P, T, H, 512], part_ml [P, T, H, 2] -> out [T, H, 512]."""
+    P, T, H, _ = (int(x) for x in part_o.shape)
+    _check("csa_shard_combine", load().csa_shard_combine(
+        P, T, H, _p(part_o), _p(part_ml), _p(sinks), _p(out), _p(dev_status), _stream(stream)))

@@ -58,6 +58,7 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     w.fcap = 2 * p.top_k + 96;
     w.off_fcand = off;   off = align_up(off + size_t(w.fslots) * w.fcap * 8, A);
     w.off_fmeta = off;   off = align_up(off + size_t(w.fslots) * 16, A);
+    w.off_shard = off;   off = align_up(off + (Tz + 2) * 8, A);
     w.data_bytes = off;
     w.total = w.state_bytes + w.data_bytes + A;
     return w;
@@ -493,6 +494,211 @@ csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *para
                                         reinterpret_cast<float *>(w + plan.off_part_o),
                                         reinterpret_cast<float *>(w + plan.off_part_ml),
                                         dev_status));
+}
+
+// ---------------------------------------------------------------- sharded decode
+
+// A shard's range of one sequence's blocks: [lo, hi), the shard's caches
+// holding hi - lo rows.
+static csa_status_t check_shard(const csa_layout_t *layout, int64_t lo, int64_t hi) {
+    if (layout->num_seqs != 1) return CSA_ERR_UNSUPPORTED;
+    if (lo < 0 || hi < lo || hi > (int64_t(1) << 31) - 1) return CSA_ERR_INVALID_ARGUMENT;
+    return CSA_OK;
+}
+
+// The shard's layout in the workspace (device arrays written by a kernel).
+static csa_layout_t shard_layout(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
+                                 const WsPlan &plan, uint8_t *w, int64_t lo, int64_t hi,
+                                 int32_t *status, cudaError_t *err) {
+    int64_t *pos = reinterpret_cast<int64_t *>(w + plan.off_shard);
+    int64_t *off = pos + (plan.T > 0 ? plan.T : 0);
+    *err = launch_shard_layout(lc, L, p.ratio, lo, hi, pos, off, status);
+    csa_layout_t S = L;
+    S.tok_pos = pos;
+    S.comp_off = off;
+    S.num_seqs = 1;
+    S.total_comp_rows = hi - lo;
+    S.max_comp_rows = hi - lo;
+    return S;
+}
+
+csa_status_t csa_shard_workspace_size(const csa_layout_t *layout, const csa_params_t *params,
+                                      int64_t shard_lo, int64_t shard_hi, size_t *bytes) {
+    if (!bytes || !layout) return CSA_ERR_INVALID_ARGUMENT;
+    CSA_TRY(check_params(params));
+    if (layout->num_tokens < 0) return CSA_ERR_INVALID_ARGUMENT;
+    CSA_TRY(check_shard(layout, shard_lo, shard_hi));
+    const size_t a = make_plan(layout->num_tokens, shard_hi - shard_lo, *params).total;
+    const size_t b = make_plan(layout->num_tokens, 0, *params).total;   // the window's partial
+    *bytes = a > b ? a : b;
+    return CSA_OK;
+}
+
+csa_status_t csa_shard_candidates(const csa_layout_t *layout, const csa_params_t *params,
+                                  int64_t shard_lo, int64_t shard_hi, const void *q_idx,
+                                  const float *w_idx, const void *k_idx_shard, float *cand_score,
+                                  int32_t *cand_idx, int32_t *n_cand, int32_t *dev_status, void *ws,
+                                  size_t ws_bytes, void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, false));
+    CSA_TRY(check_shard(layout, shard_lo, shard_hi));
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!q_idx || !w_idx || !cand_score || !cand_idx || !n_cand || !dev_status)
+        return CSA_ERR_INVALID_ARGUMENT;
+    if (shard_hi > shard_lo && !k_idx_shard) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q_idx) || (k_idx_shard && !aligned16(k_idx_shard))) return CSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = shard_hi - shard_lo;
+    const WsPlan plan = make_plan(layout->num_tokens, nb, *params);
+    CSA_TRY(check_ws(plan, ws, ws_bytes));
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    uint8_t *w = data_base(ws, ws_bytes, plan);
+    cudaError_t e = cudaSuccess;
+    if (nb == 0)   // a shard without blocks has no candidates
+        return cuda_status(launch_shard_candidates(lc, layout->num_tokens, params->top_k,
+                                                   shard_lo, nullptr, 0, nullptr, nullptr,
+                                                   cand_score, cand_idx, n_cand));
+    const csa_layout_t S = shard_layout(lc, *layout, *params, plan, w, shard_lo, shard_hi,
+                                        dev_status, &e);
+    if (e != cudaSuccess) return cuda_status(e);
+    // every visible block's score (the candidates carry them), then the local top-k
+    float *scores = reinterpret_cast<float *>(w + plan.off_scores);
+    if (one_token_per_tile(S) && decode_indexer_fits(S, sms, false))
+        e = launch_decode_indexer(lc, S, *params, q_idx, w_idx, k_idx_shard, scores, plan.ld,
+                                  dev_status, nullptr);
+    else
+        e = launch_indexer(lc, S, *params, q_idx, w_idx, k_idx_shard, scores, plan.ld, nullptr,
+                           dev_status, false);
+    if (e != cudaSuccess) return cuda_status(e);
+    int32_t *idx = reinterpret_cast<int32_t *>(w + plan.off_idx);
+    int32_t *nsel = reinterpret_cast<int32_t *>(w + plan.off_nsel);
+    TopkWs tw{static_cast<uint32_t *>(ws), reinterpret_cast<uint64_t *>(w + plan.off_slots),
+              reinterpret_cast<uint32_t *>(w + plan.off_slot_cnt)};
+    e = launch_topk(lc, S, *params, scores, plan.ld, tw, false, idx, nsel, dev_status);
+    if (e != cudaSuccess) return cuda_status(e);
+    return cuda_status(launch_shard_candidates(lc, layout->num_tokens, params->top_k, shard_lo,
+                                               scores, plan.ld, idx, nsel, cand_score, cand_idx,
+                                               n_cand));
+}
+
+csa_status_t csa_shard_merge(int32_t num_tokens, int32_t top_k, int32_t num_shards,
+                             const int64_t *shard_bounds, const float *cand_score,
+                             const int32_t *cand_idx, const int32_t *n_cand, int32_t *idx,
+                             int32_t *n_sel, int32_t *shard_idx, int32_t *shard_nsel,
+                             int32_t *dev_status, void *stream) {
+    if (num_tokens < 0 || top_k < 1 || num_shards < 1 || !shard_bounds) return CSA_ERR_INVALID_ARGUMENT;
+    if (num_shards > kMaxShards || top_k > 2048) return CSA_ERR_UNSUPPORTED;
+    for (int g = 0; g < num_shards; ++g)
+        if (shard_bounds[g] < 0 || shard_bounds[g + 1] < shard_bounds[g]) return CSA_ERR_INVALID_ARGUMENT;
+    if (shard_bounds[num_shards] > (int64_t(1) << 31) - 1) return CSA_ERR_INVALID_ARGUMENT;
+    if (num_tokens == 0) return CSA_OK;
+    if (!cand_score || !cand_idx || !n_cand || !idx || !n_sel || !shard_idx || !shard_nsel ||
+        !dev_status)
+        return CSA_ERR_INVALID_ARGUMENT;
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    ShardMergeArgs A{};
+    A.T = num_tokens;
+    A.top_k = top_k;
+    A.G = num_shards;
+    for (int g = 0; g <= num_shards; ++g) A.bounds[g] = shard_bounds[g];
+    A.cand_score = cand_score;
+    A.cand_idx = cand_idx;
+    A.n_cand = n_cand;
+    A.idx = idx;
+    A.n_sel = n_sel;
+    A.shard_idx = shard_idx;
+    A.shard_nsel = shard_nsel;
+    A.status = dev_status;
+    return cuda_status(launch_shard_merge(lc, A));
+}
+
+csa_status_t csa_shard_attention(const csa_layout_t *layout, const csa_params_t *params,
+                                 int64_t shard_lo, int64_t shard_hi, const int32_t *shard_idx,
+                                 const int32_t *shard_nsel, const void *comp_kv_shard,
+                                 const void *q, float *part_o, float *part_ml, int32_t *dev_status,
+                                 void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, false));
+    CSA_TRY(check_shard(layout, shard_lo, shard_hi));
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!shard_idx || !shard_nsel || !q || !part_o || !part_ml || !dev_status)
+        return CSA_ERR_INVALID_ARGUMENT;
+    if (shard_hi > shard_lo && !comp_kv_shard) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(part_o) || (comp_kv_shard && !aligned16(comp_kv_shard)))
+        return CSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = shard_hi - shard_lo;
+    const WsPlan plan = make_plan(layout->num_tokens, nb, *params);
+    CSA_TRY(check_ws(plan, ws, ws_bytes));
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    uint8_t *w = data_base(ws, ws_bytes, plan);
+    cudaError_t e = cudaSuccess;
+    const csa_layout_t S = shard_layout(lc, *layout, *params, plan, w, shard_lo, shard_hi,
+                                        dev_status, &e);
+    if (e != cudaSuccess) return cuda_status(e);
+    RowSource R{};
+    R.fused = kRowsSelected;
+    R.rows_per_token = params->top_k;
+    R.L = S;
+    R.ratio = params->ratio;
+    R.window = params->window;
+    R.top_k = params->top_k;
+    R.idx = shard_idx;
+    R.n_sel = shard_nsel;
+    R.comp_kv = comp_kv_shard;
+    R.no_window = 1;
+    return cuda_status(launch_attention_tc(lc, R, layout->num_tokens, *params, plan, q, nullptr,
+                                           part_o, reinterpret_cast<float *>(w + plan.off_part_o),
+                                           reinterpret_cast<float *>(w + plan.off_part_ml),
+                                           dev_status, false, part_ml));
+}
+
+csa_status_t csa_window_attention(const csa_layout_t *layout, const csa_params_t *params,
+                                  const void *q, float *part_o, float *part_ml,
+                                  int32_t *dev_status, void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_params(params));
+    CSA_TRY(check_layout(layout, params, true));
+    if (layout->num_seqs != 1) return CSA_ERR_UNSUPPORTED;
+    if (layout->num_tokens == 0) return CSA_OK;
+    if (!q || !part_o || !part_ml || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(part_o)) return CSA_ERR_INVALID_ARGUMENT;
+    const WsPlan plan = make_plan(layout->num_tokens, 0, *params, params->window);
+    CSA_TRY(check_ws(plan, ws, ws_bytes));
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    uint8_t *w = data_base(ws, ws_bytes, plan);
+    RowSource R{};
+    R.fused = kRowsSelected;
+    R.rows_per_token = params->window;
+    R.L = *layout;
+    R.ratio = params->ratio;
+    R.window = params->window;
+    R.top_k = params->top_k;
+    R.no_selected = 1;
+    return cuda_status(launch_attention_tc(lc, R, layout->num_tokens, *params, plan, q, nullptr,
+                                           part_o, reinterpret_cast<float *>(w + plan.off_part_o),
+                                           reinterpret_cast<float *>(w + plan.off_part_ml),
+                                           dev_status, false, part_ml));
+}
+
+csa_status_t csa_shard_combine(int32_t num_parts, int32_t num_tokens, int32_t n_heads,
+                               const float *part_o, const float *part_ml, const float *sinks,
+                               float *out, int32_t *dev_status, void *stream) {
+    if (num_parts < 1 || num_tokens < 0 || n_heads < 1) return CSA_ERR_INVALID_ARGUMENT;
+    if (num_parts > 128 || n_heads > 128) return CSA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return CSA_OK;
+    if (!part_o || !part_ml || !out || !dev_status) return CSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(part_o) || !aligned16(out)) return CSA_ERR_INVALID_ARGUMENT;
+    int sms = 0;
+    CSA_TRY(current_device(&sms));
+    Launch lc{static_cast<cudaStream_t>(stream), sms};
+    return cuda_status(launch_partials_combine(lc, num_parts, num_tokens, n_heads, part_o, part_ml,
+                                               sinks, out, dev_status));
 }
 
 }  // extern "C"

@@ -79,6 +79,11 @@ struct TcParams {
     float *part_ml;          // [T][splits][H][2]  (m in log2 units, l)
     int32_t *status;
     int32_t early_q;
+    int32_t raw;             // one split: write the unnormalised partial to part_o / part_ml
+    // the combine: where split s of token t, head h starts, in floats
+    // (part_o + t * po_t + s * po_s + h * 512, part_ml + t * ml_t + s * ml_s + h * 2)
+    int64_t po_t, po_s, ml_t, ml_s;
+    float *raw_ml;           // the combine: write the merged partial (out = O, raw_ml = (m, l))
 };
 
 struct TcTok;
@@ -127,7 +132,8 @@ __device__ __forceinline__ TcTok tc_token(const RowSource &R, int t) {
         k.wslot = len;
         return k;
     }
-    const int32_t ns_sel = R.fused == kRowsSelected ? R.n_sel[t] : 0;
+    // (the window's partial has no selection to read)
+    const int32_t ns_sel = (R.fused == kRowsSelected && !R.no_selected) ? R.n_sel[t] : 0;
     const TokenView v = token_view(R.L, R.ratio, t);
     k.bad = v.bad;
     if (v.bad & CSA_DEV_BAD_LAYOUT) return k;
@@ -141,10 +147,11 @@ __device__ __forceinline__ TcTok tc_token(const RowSource &R, int t) {
             ns = ns < 0 ? 0 : R.top_k;
         }
     }
+    if (R.no_selected) ns = 0;
     k.nsel = ns;
     k.wslot = (ns + 3) & ~3;
     k.first = window_first(v.pos, R.window);
-    k.nswa = static_cast<int32_t>(v.pos - k.first + 1);
+    k.nswa = R.no_window ? 0 : static_cast<int32_t>(v.pos - k.first + 1);
     k.off = v.off;
     k.n_vis = v.n_vis;
     k.b = v.b;
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             S.mh[hl] = m_ref;
             S.lh[hl] = l;
             float f = 1.f;
-            if (A.splits == 1) {
+            if (A.splits == 1 && !A.raw) {
                 float z = l;
                 if (A.sinks && hv && m_ref != -INFINITY) z += exp2f(A.sinks[h0 + hl] * kLog2e - m_ref);
                 f = (z > 0.f && l > 0.f) ? 1.f / z : 0.f;
@@ -521,10 +528,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (nch > 0) mbar_wait(&S.odone, 0, A.status);
         named_bar_sync(kBarSm, kSmThreads);
         tc_fence_after();
-        const int64_t obase = A.splits == 1
-                                  ? (static_cast<int64_t>(t) * H + h0) * kHD
-                                  : ((static_cast<int64_t>(t) * A.splits + split) * H + h0) * kHD;
-        float *dst = A.splits == 1 ? A.out : A.part_o;
+        const bool part = A.splits > 1 || A.raw;
+        const int64_t obase = part ? ((static_cast<int64_t>(t) * A.splits + split) * H + h0) * kHD
+                                   : (static_cast<int64_t>(t) * H + h0) * kHD;
+        float *dst = part ? A.part_o : A.out;
         const int hmax = min(kHG, H - h0);
         // one output column per lane: every warp store is 128 contiguous bytes
         if (nch == 0) {
@@ -546,7 +553,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
             }
         }
-        if (A.splits > 1 && !upper && hv) {
+        if (part && !upper && hv) {
             const int64_t mb = ((static_cast<int64_t>(t) * A.splits + split) * H + h0 + hl) * 2;
             A.part_ml[mb + 0] = nch > 0 ? m_ref : -INFINITY;
             A.part_ml[mb + 1] = nch > 0 ? l : 0.f;
@@ -579,8 +586,8 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
     __shared__ float inv_z;
     __shared__ float4 red[7][128];
     const int ns = A.splits;
-    const float *mlb = A.part_ml + (static_cast<int64_t>(t) * ns * A.H + h) * 2;
-    const int64_t mstride = static_cast<int64_t>(A.H) * 2;
+    const float *mlb = A.part_ml + t * A.ml_t + h * 2;
+    const int64_t mstride = A.ml_s;
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         float m[4], lv[4];
@@ -597,7 +604,7 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
         float M = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float sink = A.sinks ? A.sinks[h] * kLog2e : -INFINITY;
+        const float sink = (A.sinks && !A.raw_ml) ? A.sinks[h] * kLog2e : -INFINITY;
         const float Mall = fmaxf(M, sink);
         float z = 0.f;
 #pragma unroll
@@ -610,13 +617,20 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         if (lane == 0) {
             const bool any = M != -INFINITY;
-            if (A.sinks && any) z += exp2f(sink - Mall);
-            inv_z = (any && z > 0.f) ? 1.f / z : 0.f;
+            if (A.raw_ml) {
+                // the merged partial: O scaled to M, l = sum_s 2^(m_s - M) l_s
+                A.raw_ml[(static_cast<int64_t>(t) * A.H + h) * 2 + 0] = M;
+                A.raw_ml[(static_cast<int64_t>(t) * A.H + h) * 2 + 1] = any ? z : 0.f;
+                inv_z = 1.f;
+            } else {
+                if (A.sinks && any) z += exp2f(sink - Mall);
+                inv_z = (any && z > 0.f) ? 1.f / z : 0.f;
+            }
         }
     }
     __syncthreads();
-    const float *pb = A.part_o + (static_cast<int64_t>(t) * ns * A.H + h) * kHD + 4 * c4;
-    const int64_t pstride = static_cast<int64_t>(A.H) * kHD;
+    const float *pb = A.part_o + t * A.po_t + h * kHD + 4 * c4;
+    const int64_t pstride = A.po_s;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int base = sub; base < ns; base += kCombPer * nsub) {
         float4 v[kCombPer];
@@ -660,14 +674,14 @@ size_t attention_tc_smem_bytes() { return 1024 + kQBytes + 2 * kRowsBytes + 4 * 
 cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t T,
                                 const csa_params_t &p, const WsPlan &plan, const void *q,
                                 const float *sinks, float *out, float *part_o, float *part_ml,
-                                int32_t *status, bool early_q) {
+                                int32_t *status, bool early_q, float *raw_ml) {
     if (T <= 0) return cudaSuccess;
     CUtensorMap tq;
     const int H = p.n_heads;
     if (encode_tensor_map_2d_bf16(&tq, q, kHD, static_cast<uint64_t>(T) * H, kHD * 2, 64, kHG) !=
         CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    TcParams A;
+    TcParams A{};
     A.R = src;
     A.H = H;
     A.splits = plan.splits;
@@ -679,18 +693,53 @@ cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t 
     A.part_ml = part_ml;
     A.status = status;
     A.early_q = early_q ? 1 : 0;
+    if (raw_ml && plan.splits == 1) {
+        // one split: the kernel writes the partial straight to the caller's buffers
+        A.raw = 1;
+        A.part_o = out;
+        A.part_ml = raw_ml;
+    }
     const size_t smem = attention_tc_smem_bytes();
     cudaError_t e = set_kernel_smem(attention_tc_kernel, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.splits, (H + kHG - 1) / kHG, T);
     e = launch_pdl(attention_tc_kernel, grid, dim3(kTcThreads), smem, lc.stream, tq, A);
     if (e != cudaSuccess || plan.splits == 1) return e;
-    e = set_kernel_smem(combine_tc_kernel, 0);
-    if (e != cudaSuccess) return e;
     // splits <= kMaxSplits (the plan's cap): nsub <= 8, blockDim <= 1024
     if (plan.splits > kMaxSplits) return cudaErrorInvalidValue;
+    A.po_t = static_cast<int64_t>(plan.splits) * H * kHD;
+    A.po_s = static_cast<int64_t>(H) * kHD;
+    A.ml_t = static_cast<int64_t>(plan.splits) * H * 2;
+    A.ml_s = static_cast<int64_t>(H) * 2;
+    A.raw_ml = raw_ml;
     int nsub = (plan.splits + kCombPer - 1) / kCombPer;
     nsub = nsub < 8 ? nsub : 8;
+    e = set_kernel_smem(combine_tc_kernel, 0);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub), 0, lc.stream, A);
+}
+
+cudaError_t launch_partials_combine(const Launch &lc, int32_t P, int32_t T, int32_t H,
+                                    const float *part_o, const float *part_ml, const float *sinks,
+                                    float *out, int32_t *status) {
+    if (T <= 0) return cudaSuccess;
+    if (P < 1 || P > kMaxSplits) return cudaErrorInvalidValue;
+    TcParams A{};
+    A.H = H;
+    A.splits = P;
+    A.sinks = sinks;
+    A.out = out;
+    A.part_o = const_cast<float *>(part_o);
+    A.part_ml = const_cast<float *>(part_ml);
+    A.status = status;
+    A.po_t = static_cast<int64_t>(H) * kHD;
+    A.po_s = static_cast<int64_t>(T) * H * kHD;
+    A.ml_t = static_cast<int64_t>(H) * 2;
+    A.ml_s = static_cast<int64_t>(T) * H * 2;
+    int nsub = (P + kCombPer - 1) / kCombPer;
+    nsub = nsub < 8 ? nsub : 8;
+    cudaError_t e = set_kernel_smem(combine_tc_kernel, 0);
+    if (e != cudaSuccess) return e;
     return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub), 0, lc.stream, A);
 }
 

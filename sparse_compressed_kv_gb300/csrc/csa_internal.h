@@ -48,6 +48,7 @@ struct WsPlan {
     size_t off_scores = 0, off_slots = 0, off_slot_cnt = 0;   // offsets inside the data area
     size_t off_idx = 0, off_nsel = 0, off_part_o = 0, off_part_ml = 0;
     size_t off_fcand = 0, off_fmeta = 0;  // fused selection: candidate slots and their headers
+    size_t off_shard = 0;                 // a shard's layout: token positions [T], offsets [2]
     int32_t fslots = 0;                   // candidate slots (grid cap + tokens)
     int32_t fcap = 0;                     // entries per candidate slot
     size_t data_bytes = 0;
@@ -118,7 +119,36 @@ struct RowSource {
     const int32_t *idx;            // fused: [T][top_k]
     const int32_t *n_sel;          // fused: [T]
     const void *comp_kv;           // fused: bf16 [R][hd]
+    int32_t no_window;             // selected rows only (a shard's partial)
+    int32_t no_selected;           // window rows only (the window's partial)
 };
+
+// Sharded single-sequence decode (csa_shard.cu).
+constexpr int kMaxShards = 8;
+
+struct ShardMergeArgs {
+    int32_t T, top_k, G;
+    int32_t npad, kpad;                    // set by the launcher
+    int64_t bounds[kMaxShards + 1];        // shard g holds blocks [bounds[g], bounds[g+1])
+    const float *cand_score;               // [G][T][top_k]
+    const int32_t *cand_idx;               // [G][T][top_k] global block indices
+    const int32_t *n_cand;                 // [G][T]
+    int32_t *idx;                          // [T][top_k] global, ascending
+    int32_t *n_sel;                        // [T]
+    int32_t *shard_idx;                    // [G][T][top_k] shard rows, ascending
+    int32_t *shard_nsel;                   // [G][T]
+    int32_t *status;
+};
+
+cudaError_t launch_shard_layout(const Launch &lc, const csa_layout_t &L, int32_t ratio,
+                                int64_t lo, int64_t hi, int64_t *tok_pos_out,
+                                int64_t *comp_off_out, int32_t *status);
+cudaError_t launch_shard_candidates(const Launch &lc, int32_t T, int32_t top_k, int64_t lo,
+                                    const float *scores, int64_t ld, const int32_t *idx,
+                                    const int32_t *n_sel, float *cand_score, int32_t *cand_idx,
+                                    int32_t *n_cand);
+size_t shard_merge_smem(int G, int top_k);
+cudaError_t launch_shard_merge(const Launch &lc, ShardMergeArgs A);
 
 // k_idx: bf16 [R, 128] keys, or, with fp4, MXFP4 rows [R, 80] (csa.h).
 cudaError_t launch_indexer(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
@@ -142,11 +172,19 @@ cudaError_t launch_gather(const Launch &lc, const RowSource &src, int32_t T, voi
 
 // Shared-KV attention on the tensor cores (csa_attention_tc.cu): grid
 // (splits, ceil(H / 64), T), partials merged by a combine kernel when a
-// token has several splits.
+// token has several splits.  With raw_ml set the result is the unnormalised
+// partial instead (out: O [T][H][512] scaled to the running maximum m,
+// raw_ml: (m in log2 units, l) [T][H][2]; no sink).
 cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t T,
                                 const csa_params_t &p, const WsPlan &plan, const void *q,
                                 const float *sinks, float *out, float *part_o, float *part_ml,
-                                int32_t *status, bool early_q = false);
+                                int32_t *status, bool early_q = false, float *raw_ml = nullptr);
+
+// Log-sum-exp merge of P partials laid out [P][T][H][512] and [P][T][H][2]
+// into out [T][H][512] (with the sinks, if given, in the denominator).
+cudaError_t launch_partials_combine(const Launch &lc, int32_t P, int32_t T, int32_t H,
+                                    const float *part_o, const float *part_ml, const float *sinks,
+                                    float *out, int32_t *status);
 
 // Launch helper: programmatic dependent launch on, so each kernel's prologue
 // may overlap the previous kernel's tail (kernels wait with griddepcontrol).

@@ -327,6 +327,56 @@ def test_attention_sink_identity():
     np.testing.assert_allclose(withs[0], base[0] * factor[:, None], rtol=1e-12, atol=1e-14)
 
 
+# ----------------------------------------------- partial attention and merge
+
+def test_partials_merge_to_the_whole_attention():
+    """Cut a token's rows into random parts: the log-sum-exp merge of the
+    parts' partials equals the attention over all rows (the C oracle), with
+    and without a sink; an empty part changes nothing."""
+    rng = np.random.default_rng(12)
+    H, hd, L = 5, 64, 90
+    q = bf16_bits(rng.normal(size=(1, H, hd)) * 2)
+    rows = bf16_bits(rng.normal(size=(1, L, hd)))
+    sinks = (rng.normal(size=H) * 3).astype(np.float32)
+    full = oracle.attention(q, rows, [L], scale=0.2)
+    full_s = oracle.attention(q, rows, [L], scale=0.2, sinks=sinks)
+    for trial in range(4):
+        cuts = np.sort(rng.choice(np.arange(1, L), size=trial + 1, replace=False))
+        parts = np.split(np.arange(L), cuts)
+        parts.append(np.arange(0))                     # an empty part
+        got = [oracle.attention_partial(q[0], rows[0, p], 0.2) for p in parts]
+        O = np.stack([g[0] for g in got])
+        m = np.stack([g[1] for g in got])
+        lv = np.stack([g[2] for g in got])
+        np.testing.assert_allclose(oracle.combine_partials(O, m, lv), full[0], rtol=1e-12,
+                                   atol=1e-13)
+        np.testing.assert_allclose(oracle.combine_partials(O, m, lv, sinks=sinks), full_s[0],
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_partial_attention_closed_forms():
+    rng = np.random.default_rng(13)
+    H, hd = 3, 16
+    q = bf16_bits(rng.normal(size=(H, hd)))
+    rows = bf16_bits(rng.normal(size=(4, hd)))
+    # one row: O = the row, m = its logit, l = 1
+    O, m, lv = oracle.attention_partial(q, rows[:1], 0.5)
+    r = bits_to_f64(rows[0])
+    np.testing.assert_array_equal(lv, np.ones(H))
+    np.testing.assert_allclose(m, 0.5 * bits_to_f64(q) @ r, rtol=1e-15)
+    np.testing.assert_array_equal(O, np.repeat(r[None], H, 0))
+    # q = 0: m = 0, l = n, O = the row sum
+    O, m, lv = oracle.attention_partial(np.zeros_like(q), rows, 0.5)
+    np.testing.assert_array_equal(m, np.zeros(H))
+    np.testing.assert_array_equal(lv, np.full(H, 4.0))
+    np.testing.assert_allclose(O[1], bits_to_f64(rows).sum(0), rtol=1e-15)
+    # no rows: (0, -inf, 0), and a merge of nothing but empty parts is zero
+    O, m, lv = oracle.attention_partial(q, rows[:0], 0.5)
+    assert (m == -np.inf).all() and (lv == 0).all() and (O == 0).all()
+    np.testing.assert_array_equal(oracle.combine_partials(O[None], m[None], lv[None]),
+                                  np.zeros((H, hd)))
+
+
 # ----------------------------------------------------------- the whole step
 
 def _visible_rows(wl, t, nv):
