@@ -362,6 +362,54 @@ def ctx64k_leg(device, csa, stream, status, reps, seed):
             "l2": "hot: one layer's 4 MiB of keys and 16 MiB of rows stay in L2 across steps"}
 
 
+def decode_only_leg(args, device):
+    """Eager decode steps of one workload on two rotating layers, one stream,
+    events around --steps of them after --warmup: a short, fixed launch
+    sequence for profilers (not a bench value)."""
+    from sparse_compressed_kv_gb300 import build as cuda_build
+    from sparse_compressed_kv_gb300 import csa
+    cuda_build.build()
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    name = args.decode_only
+    if name == "hca1m":
+        wls = [W.hca1m(seed=500 + i, device=device) for i in range(2)]
+        runs = []
+        for wl in wls:
+            d = wl.to(device)
+            lay = csa.Layout(d.tok_seq, d.tok_pos, d.comp_off, d.swa_kv, d.swa_first_pos,
+                             max_comp_rows=wl.max_comp_rows,
+                             total_comp_rows=int(wl.comp_kv.shape[0]), swa_cap=wl.swa_cap)
+            prm = csa.params(wl.n_heads, 1, wl.window, wl.ratio, wl.scale)
+            runs.append((d, lay, prm, torch.empty(1, wl.n_heads, wl.hd, device=device)))
+        ws = csa.hca_workspace(runs[0][1], runs[0][2])
+
+        def step(i):
+            d, lay, prm, out = runs[i % 2]
+            csa.csa_hca_decode(lay, prm, d.comp_kv, d.q, out, status, ws, stream=stream)
+    else:
+        layers = make_layers(name, 2, device, csa, seed0=0 if name == "1m" else 77)
+        ws = csa.workspace(layers[0].layout, layers[0].prm)
+
+        def step(i):
+            L = layers[i % 2]
+            csa.csa_decode(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, L.d.comp_kv, L.d.q,
+                           L.out, status, ws, idx_out=L.idx, stream=stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    check_status(status, name)
+    return {"decode_only": name, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step_eager": round(e0.elapsed_time(e1) / args.steps, 5)}
+
+
 def prefill_leg(args, device, csa, stream, status, rank, tf_peak, peak_kind):
     """The indexer alone on a chunked-prefill workload: `args.prefill_tokens`
     query tokens of one sequence at positions 262144.. share every key tile
@@ -770,6 +818,9 @@ def main():
     ap.add_argument("--prefill-tokens", type=int, default=4096)
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill-indexer leg and print its object (for profiling)")
+    ap.add_argument("--decode-only", choices=["1m", "batch32", "hca1m"], default=None,
+                    help="run only eager decode steps of this workload (2 rotating layers) and "
+                         "print their mean time (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -787,6 +838,9 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     device = torch.device("cuda", local)
+    if args.decode_only:
+        print(json.dumps(decode_only_leg(args, device)), flush=True)
+        return
     if args.prefill_only:
         from sparse_compressed_kv_gb300 import build as cuda_build
         from sparse_compressed_kv_gb300 import csa

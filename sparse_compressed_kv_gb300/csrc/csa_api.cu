@@ -242,9 +242,9 @@ static csa_status_t indexer_scores_impl(const csa_layout_t *layout, const csa_pa
     int sms = 0;
     CSA_TRY(current_device(&sms));
     Launch lc{static_cast<cudaStream_t>(stream), sms};
-    if (!fp4 && one_token_per_tile(*layout) && decode_indexer_fits(*layout, sms, false))
+    if (one_token_per_tile(*layout) && decode_indexer_fits(*layout, sms, false))
         return cuda_status(launch_decode_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores,
-                                                 ld_scores, dev_status, nullptr));
+                                                 ld_scores, dev_status, nullptr, fp4));
     return cuda_status(launch_indexer(lc, *layout, *params, q_idx, w_idx, k_idx, scores,
                                       ld_scores, nullptr, dev_status, fp4));
 }
@@ -355,7 +355,7 @@ static cudaError_t select_blocks(const Launch &lc, const csa_layout_t &L, const 
                                  const void *q_idx, const float *w_idx, const void *k_idx,
                                  int32_t *idx, int32_t *nsel, int32_t *dev_status, bool fp4) {
     float *scores = reinterpret_cast<float *>(w + plan.off_scores);
-    if (!fp4 && one_token_per_tile(L) && decode_indexer_fits(L, lc.sm_count, true)) {
+    if (one_token_per_tile(L) && decode_indexer_fits(L, lc.sm_count, true)) {
         FusedTopk f;
         f.state = state;
         f.cand = reinterpret_cast<uint64_t *>(w + plan.off_fcand);
@@ -364,7 +364,8 @@ static cudaError_t select_blocks(const Launch &lc, const csa_layout_t &L, const 
         f.cap = plan.fcap;
         f.idx = idx;
         f.n_sel = nsel;
-        return launch_decode_indexer(lc, L, p, q_idx, w_idx, k_idx, scores, plan.ld, dev_status, &f);
+        return launch_decode_indexer(lc, L, p, q_idx, w_idx, k_idx, scores, plan.ld, dev_status, &f,
+                                     fp4);
     }
     const bool fuse = indexer_fuses_hist(L);
     cudaError_t e = launch_indexer(lc, L, p, q_idx, w_idx, k_idx, scores, plan.ld,

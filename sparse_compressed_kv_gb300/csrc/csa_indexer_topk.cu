@@ -61,6 +61,17 @@ constexpr int kABytes = 2 * kHalfBytes;        // 32 KiB per stage
 constexpr int kBoxBytes = kBoxRows * 128;      // 4 KiB: one 32-row box of one half
 constexpr int kBBytes = 2 * kN * 128;          // 16 KiB: one token's queries
 constexpr int kStageEntries = kStages * kABytes / 8;  // resolver staging in the ring
+// FP4 keys (80-byte MXFP4 rows): a ring of raw code tiles that two converter
+// warps expand into a shorter ring of f16 tiles the MMA reads; both rings fit
+// in the bf16 ring's 128 KiB, which the resolver stages in afterwards.
+constexpr int kFRow = 80;
+constexpr int kFBytes = kTileKeys * kFRow;     // 10 KiB: one raw tile
+constexpr int kFStages = 6;
+constexpr int kAStagesF = 2;
+constexpr int kScaleStages = kAStagesF + kAcc; // per-key scales, read by the epilogue
+constexpr int kConvThreads = 64;               // warps 6, 7
+constexpr int kBarConv = 4;                    // named barrier of the converter warps
+static_assert(kAStagesF * kABytes + kFStages * kFBytes <= kStages * kABytes, "FP4 rings");
 constexpr int kWarmKeys = 4 * kTileKeys;       // keys a CTA warms L2 with before its layout
 
 struct DecParams {
@@ -90,7 +101,10 @@ struct DecSmem {
     uint32_t red_or, red_max;
     int32_t fd;                        // digit found by the current search
     uint32_t fgt;                      // count above it
-    uint64_t bars[2 * kStages + 2 + 2 * kAcc];
+    uint64_t bars[40];                 // pipeline barriers (layout per key format)
+    uint64_t sfull[kScaleStages];      // FP4: a tile's key scales are written
+    float fscale[kScaleStages][kTileKeys];   // FP4: 2^(E_max - 127 + s_q) per key
+    float qmax[2];                     // FP4: the converter warps' max |q|
     uint64_t rbar;                     // the resolver's staging copies
     uint32_t rphase;
     uint32_t tmem_holder;
@@ -556,21 +570,48 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
     __syncthreads();
 }
 
-template <bool kFused>
+// f16 x2 from two e2m1 codes (the low nibble in the low half), exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
+    uint32_t d;
+    asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }"
+        : "=r"(d)
+        : "r"(byte_in_low_bits));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Instruction descriptor: kind::f16 with f16 A/B (formats 0), f32 accumulator,
+// both operands K-major, shape M x N.
+template <int M, int N>
+__device__ __forceinline__ constexpr uint32_t idesc_f16_f32() {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+template <bool kFused, bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1)
     dec_indexer_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_q, const DecParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem<1024>(smem_raw);
+    constexpr int kAst = kFp4 ? kAStagesF : kStages;   // stages of the MMA's A ring
     uint8_t *sA = smem;
+    uint8_t *sF = smem + kAStagesF * kABytes;          // FP4: raw code ring
     uint8_t *sB = smem + kStages * kABytes;
     DecSmem &S = *reinterpret_cast<DecSmem *>(sB + kBBytes);
     uint64_t *a_full = S.bars;
-    uint64_t *a_empty = a_full + kStages;
-    uint64_t *b_full = a_empty + kStages;
+    uint64_t *a_empty = a_full + kAst;
+    uint64_t *b_full = a_empty + kAst;
     uint64_t *b_empty = b_full + 1;
     uint64_t *acc_full = b_full + 2;
     uint64_t *acc_empty = acc_full + kAcc;
+    uint64_t *b_conv = acc_empty + kAcc;               // FP4: q converted to f16
+    uint64_t *f_full = b_conv + 1;                     // FP4: raw tile landed
+    uint64_t *f_empty = f_full + kFStages;             // FP4: raw tile converted
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -580,8 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c = blockIdx.x;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&a_full[s], 1);
+        for (int s = 0; s < kAst; ++s) {
+            mbar_init(&a_full[s], kFp4 ? kConvThreads : 1);
             mbar_init(&a_empty[s], 1);
         }
         mbar_init(b_full, 1);
@@ -589,6 +630,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], kEpiThreads);
+        }
+        if (kFp4) {
+            mbar_init(b_conv, kConvThreads);
+            for (int s = 0; s < kFStages; ++s) {
+                mbar_init(&f_full[s], 1);
+                mbar_init(&f_empty[s], kConvThreads);
+            }
+            for (int s = 0; s < kScaleStages; ++s) mbar_init(&S.sfull[s], kConvThreads);
         }
         mbar_init(&S.rbar, 1);
         mbar_fence_init();
@@ -623,9 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             n = n < kWarmKeys ? n : kWarmKeys;
             const int64_t r0 = u0 * kBoxRows;
             if (r0 + n > P.L.total_comp_rows) n = P.L.total_comp_rows - r0;
+            constexpr int64_t kRowB = kFp4 ? kFRow : 256;
             if (n > 0)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(P.k_idx + r0 * 256),
-                             "r"(static_cast<uint32_t>(n * 256))
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(P.k_idx + r0 * kRowB),
+                             "r"(static_cast<uint32_t>(n * kRowB))
                              : "memory");
         }
     }
@@ -672,17 +722,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cur = tl.t;
                     ++gsw;
                 }
-                const int stage = it % kStages;
-                const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-                if (!dead && !mbar_wait(&a_empty[stage], ph ^ 1u, P.status)) dead = true;
-                mbar_arrive_expect_tx(&a_full[stage], static_cast<uint32_t>(tl.nunits) * 2u * kBoxBytes);
-                uint8_t *dst = sA + stage * kABytes;
-                const int32_t row0 = static_cast<int32_t>(row_base + tl.s0);
-                for (int bx = 0; bx < tl.nunits; ++bx) {
-                    tma_load_2d(dst + bx * kBoxBytes, &tm_k, 0, row0 + bx * kBoxRows, &a_full[stage],
-                                pol_k);
-                    tma_load_2d(dst + kHalfBytes + bx * kBoxBytes, &tm_k, 64, row0 + bx * kBoxRows,
-                                &a_full[stage], pol_k);
+                if constexpr (kFp4) {
+                    // the tile's rows are contiguous: one bulk copy (clamped at
+                    // the cache's end; rows past it are never scored)
+                    const int fs = it % kFStages;
+                    const uint32_t ph = static_cast<uint32_t>(it / kFStages) & 1u;
+                    if (!dead && !mbar_wait(&f_empty[fs], ph ^ 1u, P.status)) dead = true;
+                    const int64_t r0 = row_base + tl.s0;
+                    int64_t nr = static_cast<int64_t>(tl.nunits) * kBoxRows;
+                    if (r0 + nr > P.L.total_comp_rows) nr = P.L.total_comp_rows - r0;
+                    const uint32_t bytes = static_cast<uint32_t>(nr * kFRow);
+                    mbar_arrive_expect_tx(&f_full[fs], bytes);
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+                        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(sF + fs * kFBytes)),
+                        "l"(P.k_idx + r0 * kFRow), "r"(bytes), "r"(smem_addr(&f_full[fs])), "l"(pol_k)
+                        : "memory");
+                } else {
+                    const int stage = it % kStages;
+                    const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+                    if (!dead && !mbar_wait(&a_empty[stage], ph ^ 1u, P.status)) dead = true;
+                    mbar_arrive_expect_tx(&a_full[stage], static_cast<uint32_t>(tl.nunits) * 2u * kBoxBytes);
+                    uint8_t *dst = sA + stage * kABytes;
+                    const int32_t row0 = static_cast<int32_t>(row_base + tl.s0);
+                    for (int bx = 0; bx < tl.nunits; ++bx) {
+                        tma_load_2d(dst + bx * kBoxBytes, &tm_k, 0, row0 + bx * kBoxRows, &a_full[stage],
+                                    pol_k);
+                        tma_load_2d(dst + kHalfBytes + bx * kBoxBytes, &tm_k, 64, row0 + bx * kBoxRows,
+                                    &a_full[stage], pol_k);
+                    }
                 }
                 ++it;
             }
@@ -690,7 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0 && ua < ub) {
-            constexpr uint32_t idesc = idesc_bf16_f32<kTileKeys, kN>();
+            constexpr uint32_t idesc =
+                kFp4 ? idesc_f16_f32<kTileKeys, kN>() : idesc_bf16_f32<kTileKeys, kN>();
             int t = token_of(S.U, T, ua), cur = -1;
             int64_t u = ua;
             uint32_t gsw = 0;
@@ -701,7 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             Tile tl;
             while (next_tile(S.U, ub, t, u, tl)) {
                 if (tl.t != cur) {
-                    if (!dead && !mbar_wait(b_full, gsw & 1u, P.status)) dead = true;
+                    // FP4: the converter warps turn the token's q into f16 first
+                    if (!dead && !mbar_wait(kFp4 ? b_conv : b_full, gsw & 1u, P.status)) dead = true;
                     cur = tl.t;
                     ++gsw;
                 }
@@ -709,8 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!dead && !mbar_wait(&acc_empty[acc], (static_cast<uint32_t>(it / kAcc) & 1u) ^ 1u,
                                         P.status))
                     dead = true;
-                const int stage = it % kStages;
-                const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+                const int stage = it % kAst;
+                const uint32_t ph = static_cast<uint32_t>(it / kAst) & 1u;
                 if (!dead && !mbar_wait(&a_full[stage], ph, P.status)) dead = true;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kN);
@@ -751,6 +821,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) tmem_ld16(col + c4 * 16, v[c4]);
             tmem_wait_ld();
+            // FP4: the key's scale 2^(E_max - 127 + s_q), read before the
+            // accumulator goes back (the converters reuse the slot after that)
+            float ksc = 1.f;
+            if constexpr (kFp4) {
+                const int ss = it % kScaleStages;
+                const bool ok2 =
+                    dead || mbar_wait(&S.sfull[ss], static_cast<uint32_t>(it / kScaleStages) & 1u, P.status);
+                if (!__all_sync(0xffffffffu, ok2)) dead = true;
+                ksc = S.fscale[ss][row];
+            }
             // the accumulator is in registers: hand it back before the math
             tc_fence_before();
             mbar_arrive(&acc_empty[acc]);
@@ -779,7 +859,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 16; ++i)
                         part[c4] = fmaf(__ldg(wt + c4 * 16 + i), fmaxf(v[c4][i], 0.f), part[c4]);
             }
-            const float score = (part[0] + part[1]) + (part[2] + part[3]);
+            // (FP4: relu(c x) = c relu(x) for the positive key scale c)
+            const float score = ((part[0] + part[1]) + (part[2] + part[3])) * ksc;
             if (valid && CSA_CHECK(s < P.ld, P.status)) P.scores[static_cast<int64_t>(tk) * P.ld + s] = score;
             if (kFused) {
                 const uint32_t key = score_key(score);
@@ -802,7 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++it;
         }
         if (kFused && !slots_ready) named_bar_sync(kBarSlots, kEpiThreads + 64);
-    } else if (kFused) {
+    } else {
+      if constexpr (kFused) {
         // ------------------------------------------------ slot table (warps 6, 7)
         // candidate slots: one per (token, CTA that owns part of it)
         const int at = tid - 192;
@@ -823,7 +905,137 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (at == 0 && (S.sb[T] > P.f.slots || (ub - ua) * kBoxRows > kSegKeysMax))
             raise_status(P.status, CSA_DEV_CAPACITY);   // the host plan rules this out
-        named_bar_sync(kBarSlots, kEpiThreads + 64);
+        // the epilogue waits for the table; these warps go on (FP4: to convert)
+        named_bar_arrive(kBarSlots, kEpiThreads + 64);
+      }
+      if constexpr (kFp4) {
+        // ------------------------------------------------ FP4 converters (warps 6, 7)
+        // The token's q: bf16 -> f16 in place, scaled by 2^-s_q so that it
+        // stays below f16's largest value.  A key tile: the e2m1 codes of
+        // each block b scaled by 2^(E_b - E_max) in f16 (exact: an e2m1 value
+        // times a power of two >= 2^-24 is an f16 value; blocks more than 24
+        // binades below the key's largest contribute below f16's range and
+        // are dropped), laid out as the bf16 tiles are (128-byte swizzle,
+        // K-major); the per-key factor 2^(E_max - 127 + s_q) goes to the
+        // epilogue.
+        const int ct = tid - 192;
+        const int cw = warp - 6;
+        int t = ua < ub ? token_of(S.U, T, ua) : 0, cur = -1;
+        int64_t u = ua;
+        uint32_t gsw = 0;
+        int it = 0;
+        bool dead = false;
+        int qs = 0;
+        Tile tl;
+        while (next_tile(S.U, ub, t, u, tl)) {
+            if (tl.t != cur) {
+                const bool ok = dead || mbar_wait(b_full, gsw & 1u, P.status);
+                if (!__all_sync(0xffffffffu, ok)) dead = true;
+                uint4 *qv = reinterpret_cast<uint4 *>(sB) + ct * (kBBytes / 16 / kConvThreads);
+                constexpr int kQv = kBBytes / 16 / kConvThreads;   // 16 x 16 bytes per thread
+                uint4 w[kQv];
+                float mx = 0.f;
+#pragma unroll
+                for (int j = 0; j < kQv; ++j) {
+                    w[j] = qv[j];
+                    const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        mx = fmaxf(mx, fabsf(__uint_as_float(ww[e] << 16)));
+                        mx = fmaxf(mx, fabsf(__uint_as_float(ww[e] & 0xFFFF0000u)));
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0) S.qmax[cw] = mx;
+                named_bar_sync(kBarConv, kConvThreads);
+                mx = fmaxf(S.qmax[0], S.qmax[1]);
+                qs = mx >= 32768.f ? ilogbf(mx) - 14 : 0;
+                const float f = ldexpf(1.f, -qs);
+#pragma unroll
+                for (int j = 0; j < kQv; ++j) {
+                    const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 h2 = __floats2half2_rn(__uint_as_float(ww[e] << 16) * f,
+                                                             __uint_as_float(ww[e] & 0xFFFF0000u) * f);
+                        o[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                    }
+                    qv[j] = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                named_bar_sync(kBarConv, kConvThreads);   // S.qmax is read by both warps first
+                fence_proxy_async_smem();
+                mbar_arrive(b_conv);
+                cur = tl.t;
+                ++gsw;
+            }
+            const int fs = it % kFStages;
+            const int as = it % kAStagesF;
+            const int ss = it % kScaleStages;
+            bool ok = dead || mbar_wait(&f_full[fs], static_cast<uint32_t>(it / kFStages) & 1u, P.status);
+            ok = ok && (dead || mbar_wait(&a_empty[as], (static_cast<uint32_t>(it / kAStagesF) & 1u) ^ 1u,
+                                          P.status));
+            if (!__all_sync(0xffffffffu, ok)) dead = true;
+            const int nrows = tl.nunits * kBoxRows;
+            const uint8_t *fa = sF + fs * kFBytes;
+            uint8_t *dA = sA + as * kABytes;
+            for (int r = ct; r < kTileKeys; r += kConvThreads) {
+                if (r >= nrows) {
+                    S.fscale[ss][r] = 0.f;   // not a key of this tile: never scored
+                    continue;
+                }
+                const uint8_t *row = fa + r * kFRow;
+                uint32_t cw32[16];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * q4);
+                    cw32[4 * q4 + 0] = v.x;
+                    cw32[4 * q4 + 1] = v.y;
+                    cw32[4 * q4 + 2] = v.z;
+                    cw32[4 * q4 + 3] = v.w;
+                }
+                const uint32_t ev = *reinterpret_cast<const uint32_t *>(row + 64);
+                int eb[4];
+                int emax = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    eb[b] = static_cast<int>((ev >> (8 * b)) & 0xFFu);
+                    emax = eb[b] > emax ? eb[b] : emax;
+                }
+                // 2^-dlt as an f16 pair: normal down to 2^-14, subnormal to 2^-24
+                uint32_t scb[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int dlt = emax - eb[b];
+                    const uint32_t hb = dlt <= 14 ? static_cast<uint32_t>(15 - dlt) << 10
+                                                  : (dlt <= 24 ? 1u << (24 - dlt) : 0u);
+                    scb[b] = hb | (hb << 16);
+                }
+                // 2^(emax - 127 + qs) as an f32 (2^-127, the one subnormal case, when both are 0)
+                S.fscale[ss][r] =
+                    emax + qs >= 1 ? __int_as_float((emax + qs) << 23) : __int_as_float(1 << 22);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    // elements 8j .. 8j + 7 (code bytes 4j .. 4j + 3) of block j / 4
+                    const uint32_t wd = cw32[j];
+                    const uint32_t sc = scb[j >> 2];
+                    const uint32_t o0 = hmul2_bits(e2m1x2_to_f16x2(wd), sc);
+                    const uint32_t o1 = hmul2_bits(e2m1x2_to_f16x2(wd >> 8), sc);
+                    const uint32_t o2 = hmul2_bits(e2m1x2_to_f16x2(wd >> 16), sc);
+                    const uint32_t o3 = hmul2_bits(e2m1x2_to_f16x2(wd >> 24), sc);
+                    const int hh = j >> 3, c8 = j & 7;
+                    *reinterpret_cast<uint4 *>(dA + hh * kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+                        make_uint4(o0, o1, o2, o3);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&a_full[as]);
+            mbar_arrive(&f_empty[fs]);
+            mbar_arrive(&S.sfull[ss]);
+            ++it;
+        }
+      }
     }
 
     if (kFused && ua < ub) {
@@ -870,17 +1082,17 @@ bool decode_indexer_fits(const csa_layout_t &L, int sm_count, bool fused) {
 cudaError_t launch_decode_indexer(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
                                   const void *q_idx, const float *w_idx, const void *k_idx,
                                   float *scores, int64_t ld, int32_t *status,
-                                  const FusedTopk *fused) {
+                                  const FusedTopk *fused, bool fp4) {
     const int T = L.num_tokens;
     if (T <= 0) return cudaSuccess;
     CUtensorMap tk, tq;
-    if (L.total_comp_rows > 0) {
+    if (L.total_comp_rows > 0 && !fp4) {
         if (encode_tensor_map_2d_bf16(&tk, k_idx, kIHD, static_cast<uint64_t>(L.total_comp_rows),
                                       kIHD * 2, 64, kBoxRows) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     } else {
-        // no cache rows at all: a map over the queries keeps the argument
-        // valid; no key tile is ever loaded (every token selects nothing)
+        // FP4 keys come by bulk copies, and with no cache rows at all no key
+        // tile is ever loaded: a map over the queries keeps the argument valid
         if (encode_tensor_map_2d_bf16(&tk, q_idx, kIHD, static_cast<uint64_t>(T) * kNIH, kIHD * 2,
                                       64, kBoxRows) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
@@ -901,13 +1113,8 @@ cudaError_t launch_decode_indexer(const Launch &lc, const csa_layout_t &L, const
     P.f = fused ? *fused : FusedTopk{};
     const size_t smem = dec_smem_bytes();
     const int grid = dec_grid(L, lc.sm_count);
-    if (fused) {
-        auto kern = dec_indexer_kernel<true>;
-        cudaError_t e = set_kernel_smem(kern, smem);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, lc.stream, tk, tq, P);
-    }
-    auto kern = dec_indexer_kernel<false>;
+    auto kern = fused ? (fp4 ? dec_indexer_kernel<true, true> : dec_indexer_kernel<true, false>)
+                      : (fp4 ? dec_indexer_kernel<false, true> : dec_indexer_kernel<false, false>);
     cudaError_t e = set_kernel_smem(kern, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, lc.stream, tk, tq, P);

@@ -103,7 +103,7 @@ bool decode_indexer_fits(const csa_layout_t &L, int sm_count, bool fused);
 cudaError_t launch_decode_indexer(const Launch &lc, const csa_layout_t &L, const csa_params_t &p,
                                   const void *q_idx, const float *w_idx, const void *k_idx,
                                   float *scores, int64_t ld, int32_t *status,
-                                  const FusedTopk *fused);
+                                  const FusedTopk *fused, bool fp4 = false);
 
 // Where attention rows come from.
 enum RowMode { kRowsGathered = 0, kRowsSelected = 1, kRowsAllVisible = 2 };
