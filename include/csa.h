@@ -268,7 +268,7 @@ csa_status_t csa_hca_decode(const csa_layout_t *layout, const csa_params_t *para
  * csa_window_attention: the window rows of every token (from the layout's
  * ring), as a partial of the same form.
  * csa_shard_combine: num_parts partials laid out [P][T][H][512] and
- * [P][T][H][2] (P <= 128) -> out f32 [T, H, 512]; a partial with m = -inf
+ * [P][T][H][2] (P <= 256) -> out f32 [T, H, 512]; a partial with m = -inf
  * carries no rows. */
 csa_status_t csa_shard_workspace_size(const csa_layout_t *layout, const csa_params_t *params,
                                       int64_t shard_lo, int64_t shard_hi,

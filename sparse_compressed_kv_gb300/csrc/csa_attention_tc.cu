@@ -262,6 +262,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_launch_dependents();
     if (!A.early_q && tid == 0) load_q();
 
+    // The fetch warps load the selection entries of their first chunk's rows
+    // now, in the same round trip as the token record (entries past the
+    // token's selection count are read but not used).
+    const bool fetch_warp = warp == 0 || warp >= 6;
+    int32_t pre_sidx = -1;
+    if (fetch_warp && A.R.fused == kRowsSelected && !A.R.no_selected) {
+        const int li = warp == 0 ? 0 : warp - 5;
+        const int j = split * A.rows_split + kLdRows * li + lane;
+        if (lane < kLdRows && j < A.R.top_k) pre_sidx = A.R.idx[static_cast<int64_t>(t) * A.R.top_k + j];
+    }
     // the token's row slots (one reader, shared)
     __shared__ TcTok tok_s;
     if (tid == 0) {
@@ -331,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             umma_commit(&S.odone);
         }
-    } else if (warp == 0 || warp >= 6) {
+    } else if (fetch_warp) {
         // ------------------------------------------------ row fetch
         const TcTok k = tok_s;
         const int li = warp == 0 ? 0 : warp - 5;   // rows kLdRows li .. of each chunk
@@ -350,7 +360,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 } else if (j < k.nsel) {
                     const int32_t sidx = A.R.fused == kRowsAllVisible
                                              ? j
-                                             : A.R.idx[static_cast<int64_t>(t) * A.R.top_k + j];
+                                             : (i == 0 ? pre_sidx
+                                                       : A.R.idx[static_cast<int64_t>(t) * A.R.top_k + j]);
                     if (sidx < 0 || sidx >= k.n_vis) bad |= CSA_DEV_BAD_INDEX;
                     else if (CSA_CHECK(k.off + sidx < A.R.L.total_comp_rows, A.status))
                         src = static_cast<const __nv_bfloat16 *>(A.R.comp_kv) + (k.off + sidx) * kHD;
@@ -573,7 +584,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // loaded kCombPer at a time (all of them in flight), and the nsub partial
 // sums meet in shared memory in a fixed order.
 constexpr int kCombPer = 8;
-constexpr int kMaxSplits = 128;
+constexpr int kMaxSplits = 256;
+constexpr int kMlPer = kMaxSplits / 32;    // (m, l) pairs per lane of the first warp
 
 __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
     pdl_wait();
@@ -590,9 +602,9 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
     const int64_t mstride = A.ml_s;
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        float m[4], lv[4];
+        float m[kMlPer], lv[kMlPer];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kMlPer; ++k) {
             m[k] = -INFINITY;
             lv[k] = 0.f;
             if (lane + 32 * k < ns) {
@@ -601,14 +613,16 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
                 lv[k] = x.y;
             }
         }
-        float M = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+        float M = m[0];
+#pragma unroll
+        for (int k = 1; k < kMlPer; ++k) M = fmaxf(M, m[k]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         const float sink = (A.sinks && !A.raw_ml) ? A.sinks[h] * kLog2e : -INFINITY;
         const float Mall = fmaxf(M, sink);
         float z = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kMlPer; ++k) {
             const float w = m[k] == -INFINITY ? 0.f : exp2f(m[k] - Mall);
             if (lane + 32 * k < ns) wgt[lane + 32 * k] = w;
             z += w * lv[k];
