@@ -40,8 +40,8 @@ UNIT = "tokens/s/layer"
 # committed ncu capture of that step (profiles/), and the SHA-256 prefix of the
 # kernel source it was taken on: once the source changes the figure no longer
 # describes the kernel, and the roofline reports traffic null.
-SELECT_TRAFFIC_BYTES = 67234816 + 212224
-SELECT_TRAFFIC_SOURCE = "97b7b5edf4290963"
+SELECT_TRAFFIC_BYTES = 67238656 + 128256
+SELECT_TRAFFIC_SOURCE = "2127d4d4c80e3177"
 
 
 def select_traffic():
@@ -256,41 +256,69 @@ def check_status(status, where):
         raise RuntimeError(f"device status {st:#x} in the {where} region")
 
 
-def e2e_leg(layers, step, stream, steps, warmup, world, depth=3):
+def e2e_leg(layers, step, stream, steps, warmup, world):
     """The step through the public API with host buffers: every step copies
     its activations from pinned host memory, runs csa_decode and copies the
-    output back to pinned host memory, all inside the timed region.  Up to
-    `depth` steps are in flight (a serving loop's pipelining): step i waits
-    for the output of step i - depth before reusing its host buffer."""
+    output back to pinned host memory, all inside the timed region.  As a
+    serving loop overlaps them, one CUDA graph holds one step per rotating
+    layer: the input copies on their own stream (ahead of the decode that
+    reads them), each csa_decode on the main stream, each output copy on a
+    third stream right behind its decode; value = steps / time over whole
+    replays."""
+    nl = len(layers)
     hin = [(L.d.q_idx.cpu().pin_memory(), L.d.w_idx.cpu().pin_memory(),
             L.d.q.cpu().pin_memory()) for L in layers]
-    hout = [torch.empty(layers[0].out.shape, dtype=torch.float32).pin_memory()
-            for _ in range(depth)]
-    done = [torch.cuda.Event() for _ in range(depth)]
-    n = max(3, steps)
-    with torch.cuda.stream(stream):
-        for i in range(warmup + n):
-            if i == warmup:
-                stream.synchronize()
-                t_start = time.perf_counter()
-            slot = i % depth
-            if i >= depth:
-                done[slot].synchronize()
-            L = layers[i % len(layers)]
-            hq_idx, hw_idx, hq = hin[i % len(layers)]
-            L.d.q_idx.copy_(hq_idx, non_blocking=True)
-            L.d.w_idx.copy_(hw_idx, non_blocking=True)
-            L.d.q.copy_(hq, non_blocking=True)
+    hout = [torch.empty(layers[0].out.shape, dtype=torch.float32).pin_memory() for _ in layers]
+    s_in = torch.cuda.Stream(device=stream.device)
+    s_out = torch.cuda.Stream(device=stream.device)
+
+    def pipeline():
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        h2d = [torch.cuda.Event() for _ in layers]
+        dec = [torch.cuda.Event() for _ in layers]
+        for j, L in enumerate(layers):
+            hq_idx, hw_idx, hq = hin[j]
+            with torch.cuda.stream(s_in):
+                L.d.q_idx.copy_(hq_idx, non_blocking=True)
+                L.d.w_idx.copy_(hw_idx, non_blocking=True)
+                L.d.q.copy_(hq, non_blocking=True)
+                h2d[j].record(s_in)
+            stream.wait_event(h2d[j])
             step(L, stream)
-            hout[slot].copy_(L.out, non_blocking=True)
-            done[slot].record(stream)
+            dec[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(dec[j])
+                hout[j].copy_(L.out, non_blocking=True)
+        join_in, join_out = torch.cuda.Event(), torch.cuda.Event()
+        join_in.record(s_in)
+        join_out.record(s_out)
+        stream.wait_event(join_in)
+        stream.wait_event(join_out)
+    with torch.cuda.stream(stream):
+        pipeline()
+    torch.cuda.synchronize()
+    g = capture(pipeline, stream)
+    reps = max(1, (max(3, steps) + nl - 1) // nl)
+    wreps = max(1, (warmup + nl - 1) // nl)
+    with torch.cuda.stream(stream):
+        for _ in range(wreps):
+            g.replay()
+        torch.cuda.synchronize()
+        t_start = time.perf_counter()
+        for _ in range(reps):
+            g.replay()
         stream.synchronize()
-    e2e_ms = (time.perf_counter() - t_start) * 1e3 / n
+    e2e_ms = (time.perf_counter() - t_start) * 1e3 / (reps * nl)
     hq_idx, hw_idx, hq = hin[0]
-    h2d = hq_idx.numel() * 2 + hw_idx.numel() * 4 + hq.numel() * 2
+    h2d_b = hq_idx.numel() * 2 + hw_idx.numel() * 4 + hq.numel() * 2
     return {"value": round(world * 1e3 / e2e_ms, 1), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout[0].numel() * 4),
-            "ms_per_step": round(e2e_ms, 5), "in_flight": depth}
+            "h2d_bytes_per_step": int(h2d_b), "d2h_bytes_per_step": int(hout[0].numel() * 4),
+            "ms_per_step": round(e2e_ms, 5), "steps_timed": reps * nl,
+            "launch": f"one CUDA graph of {nl} steps: input copies on one stream, csa_decode on "
+                      "another, each output copy on a third behind its decode"}
 
 
 def ctx64k_leg(device, csa, stream, status, reps, seed):
