@@ -295,13 +295,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t q_base = smem_addr(sQ);
             const uint32_t r_base = smem_addr(sRows);
             const uint32_t p_base = smem_addr(sP);
-            // S = Q . rows^T of chunk i, into S buffer i % 2
+            // S = Q . rows^T of chunk i, into S buffer i % 2 (rows landed,
+            // the S buffer read by the softmax)
             auto qk = [&](int i) {
                 const int st = i & 1;
-                const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
-                mbar_wait(&S.full[st], ph, A.status);
-                mbar_wait(&S.sfree[st], ph ^ 1u, A.status);
-                tc_fence_after();
                 const uint32_t rows = r_base + st * kRowsBytes;
 #pragma unroll
                 for (int kk = 0; kk < 32; ++kk) {
@@ -312,17 +309,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 umma_commit(&S.sfull[st]);
             };
-            // QK^T of the next chunk goes out before PV of this one, so it
-            // runs while the softmax of this chunk does
-            qk(0);
-            for (int i = 0; i < nch; ++i) {
-                if (i + 1 < nch) qk(i + 1);
+            // O^T[d][h] += sum_j rows[j][d] P[h][j] of chunk i (P written),
+            // per 128-column tile of d
+            auto pv = [&](int i) {
                 const int st = i & 1;
-                const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
                 const uint32_t rows = r_base + st * kRowsBytes;
-                mbar_wait(&S.pfull[st], ph, A.status);
-                tc_fence_after();
-                // O^T[d][h] += sum_j rows[j][d] P[h][j], per 128-column tile of d
                 const uint32_t pb = p_base + st * 2 * kPBytes;
 #pragma unroll
                 for (int dt = 0; dt < 4; ++dt)
@@ -338,6 +329,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 umma_commit(&S.empty[st]);
                 umma_commit(&S.pfree[st]);
+            };
+            // Issue whichever is ready: QK^T of chunk nq (at most one chunk
+            // ahead of PV, so it runs during the softmax of chunk nq - 1) or
+            // PV of chunk np.  PV does not wait behind a QK^T whose rows are
+            // still in flight (those rows wait for the PV two chunks back).
+            // Every poll is bounded: after the wait limit the status word gets
+            // CSA_DEV_TIMEOUT and the rest is issued without waiting.
+            int nq = 0, np = 0;
+            bool dead = false;
+            uint32_t polls = 0;
+            uint64_t t_start = 0;
+            while (np < nch) {
+                bool did = false;
+                if (nq < nch && nq <= np + 1) {
+                    const int st = nq & 1;
+                    const uint32_t ph = static_cast<uint32_t>(nq >> 1) & 1u;
+                    if (dead || (mbar_try_wait(&S.full[st], ph) && mbar_try_wait(&S.sfree[st], ph ^ 1u))) {
+                        tc_fence_after();
+                        qk(nq++);
+                        did = true;
+                    }
+                }
+                if (!did && np < nq) {
+                    const int st = np & 1;
+                    const uint32_t ph = static_cast<uint32_t>(np >> 1) & 1u;
+                    if (dead || mbar_try_wait(&S.pfull[st], ph)) {
+                        tc_fence_after();
+                        pv(np++);
+                        did = true;
+                    }
+                }
+                if (did) {
+                    polls = 0;
+                } else if (++polls == 1) {
+                    t_start = global_timer_ns();
+                } else if ((polls & 1023u) == 0 && global_timer_ns() - t_start > kWaitNs) {
+                    raise_status(A.status, CSA_DEV_TIMEOUT);
+                    dead = true;
+                }
             }
             umma_commit(&S.odone);
         }
