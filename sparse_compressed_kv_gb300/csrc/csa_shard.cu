@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kMergeThreads) shard_merge_kernel(const ShardM
     for (int i = threadIdx.x; i < kpad; i += blockDim.x)
         sel[i] = i < kk ? 0xffffffffu - static_cast<uint32_t>(mkeys[i] & 0xffffffffu) : 0xffffffffu;
     __syncthreads();
-    // ascending sort of kpad 32-bit values: the descending sort of their complements
+    // ascending bitonic sort of the kpad block indices
     for (int k = 2; k <= kpad; k <<= 1)
         for (int j = k >> 1; j > 0; j >>= 1) {
             for (int i = threadIdx.x; i < kpad; i += blockDim.x) {

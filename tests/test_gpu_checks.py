@@ -1,8 +1,8 @@
 """The build with internal bounds checks (libcsa_checks.so, CSA_CHECKS=1).
 
 Every bounds check inside the library must hold on the parity and full-size
-workloads: the GPU parity tests run again in a child process that loads the
-checked build, and they require a zero status word (a failed check would set
+workloads: the GPU parity, HCA, sharded-decode and FP4 tests run again in a
+child process that loads the checked build, and they require a zero status word (a failed check would set
 CSA_DEV_CHECK) besides their usual comparisons with the oracle.
 """
 import os
@@ -26,6 +26,7 @@ def test_parity_suite_under_the_checked_build(cuda_device):
     assert which.stdout.strip().endswith("libcsa_checks.so"), which.stdout + which.stderr
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
            os.path.join("tests", "test_gpu_parity.py"), os.path.join("tests", "test_gpu_hca.py"),
+           os.path.join("tests", "test_gpu_shard.py"), os.path.join("tests", "test_gpu_fp4.py"),
            os.path.join("tests", "test_gpu_full_size.py") + "::test_batch32_decode"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     tail = (r.stdout + r.stderr)[-3000:]
