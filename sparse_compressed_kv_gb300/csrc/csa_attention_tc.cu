@@ -585,13 +585,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int hb = 0; hb < 4; ++hb) tmem_ld16_raw(tmem + lane_off + kOCol + dt * kHG + hb * 16, r[hb]);
                 tmem_wait_ld();
+                float *dd = dst + obase + d;
+                if (part && hmax == kHG) {
+                    // a raw partial of a full head group: no scale, no head bound
 #pragma unroll
-                for (int hb = 0; hb < 4; ++hb)
+                    for (int hb = 0; hb < 4; ++hb)
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int h = hb * 16 + c;
-                        if (h < hmax) dst[obase + h * kHD + d] = __uint_as_float(r[hb][c]) * S.fin[h];
-                    }
+                        for (int c = 0; c < 16; ++c) dd[(hb * 16 + c) * kHD] = __uint_as_float(r[hb][c]);
+                } else {
+#pragma unroll
+                    for (int hb = 0; hb < 4; ++hb)
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int h = hb * 16 + c;
+                            if (h < hmax) dd[h * kHD] = __uint_as_float(r[hb][c]) * S.fin[h];
+                        }
+                }
             }
         }
         if (part && !upper && hv) {
