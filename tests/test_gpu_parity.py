@@ -62,6 +62,26 @@ def test_grouped_tokens_single_sequence(cuda_device):
     full_chain(H.Run(wl, cuda_device))
 
 
+SHAPE_CASES = {
+    # the largest top_k the library takes, two sequences
+    "topk2048": lambda: W.make("k2048", seed=41, seq_lens=[4 * 20000, 4 * 9000],
+                               n_comp=[20000, 9000], top_k=2048, n_heads=64),
+    # another compression ratio and a shorter window (visibility and window
+    # arithmetic away from ratio 4 / window 128)
+    "ratio8_window64": lambda: W.make("r8w64", seed=42, seq_lens=[8 * 3000 + 5, 8 * 700],
+                                      tokens=[1, 2], n_comp=[3000, 700], top_k=256, n_heads=32,
+                                      ratio=8, window=64, swa_cap=96),
+    # two head groups per token
+    "heads128": lambda: W.make("h128", seed=43, seq_lens=[4 * 6000, 4 * 2500],
+                               n_comp=[6000, 2500], top_k=512, n_heads=128),
+}
+
+
+@pytest.mark.parametrize("name", list(SHAPE_CASES))
+def test_other_shapes(cuda_device, name):
+    full_chain(H.Run(SHAPE_CASES[name](), cuda_device))
+
+
 def test_topk_covers_everything_and_empty(cuda_device):
     # token 0: position 2 -> no visible block (window only)
     # token 1: top_k >= n_vis -> every visible block, attention is dense
