@@ -136,7 +136,7 @@ class Layer:
 def algorithmic_bytes(wl: W.Workload):
     """Bytes the method must move for one step: the visible indexer keys, the
     selected and window rows, the token's activations and its f32 output."""
-    keys = rows = 0
+    keys = rows = scores = 0
     T = wl.num_tokens
     for t in range(T):
         b = int(wl.tok_seq[t])
@@ -144,11 +144,16 @@ def algorithmic_bytes(wl: W.Workload):
         p = int(wl.tok_pos[t])
         nv = min(n_comp, p // wl.ratio)
         keys += nv * wl.ihd * 2
+        scores += nv * 4
         rows += (min(wl.top_k, nv) + min(wl.window, p + 1)) * wl.hd * 2
     act = T * (wl.n_ih * wl.ihd * 2 + wl.n_ih * 4 + wl.n_heads * wl.hd * 2)
     out = T * wl.n_heads * wl.hd * 4
+    # the unfused API's extra traffic: the f32 score row written and read back
+    # by the top-k, and the gathered rows written and read back by the attention
+    unfused_extra = 2 * scores + 2 * rows
     return {"indexer": keys + T * (wl.n_ih * wl.ihd * 2 + wl.n_ih * 4),
-            "step": keys + rows + act + out, "keys": keys, "rows": rows}
+            "step": keys + rows + act + out, "keys": keys, "rows": rows,
+            "unfused_extra": unfused_extra}
 
 
 def make_layers(name: str, n_layers: int, device, csa, seed0: int):
@@ -703,6 +708,7 @@ def run_ours(args, rank, world, device):
                                  "kernel_ms": round(idx_ms, 5),
                                  "kernel_ms_blocks": spread(idx_blocks)},
         "indexer_keys_per_s": round(n_vis0 / (idx_ms * 1e-3), 1),
+        "unfused_extra_bytes_per_step": ab["unfused_extra"],
         "step_roofline": {"bound": "hbm", "algorithmic_bytes": ab["step"],
                           "achieved": round(ab["step"] / (ms * 1e-3) / 1e9, 1),
                           "peak": hbm_peak, "unit": "GB/s",
