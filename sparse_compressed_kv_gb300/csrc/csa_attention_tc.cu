@@ -169,16 +169,6 @@ __device__ __forceinline__ void tmem_ld16_raw(uint32_t taddr, uint32_t (&r)[16])
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_st16_raw(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15])
-        : "memory");
-}
-
 // 2^x with the hardware's approximate exponential (relative error about
 // 2^-22, far below the bf16 terms P is stored in); 2^-inf = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -187,9 +177,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-__device__ __forceinline__ void tmem_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 
 // Shared-memory descriptor with explicit leading / stride byte offsets
 // (128-byte swizzle).  K-major: the stride is the step between 8-row groups.
@@ -514,7 +501,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 16; ++c)
                             r[c] = __float_as_uint(__uint_as_float(r[c]) * S.alpha[hb * 16 + c]);
-                        tmem_st16_raw(ta, r);
+                        tmem_st16(ta, r);
                     }
                 tmem_wait_st();
                 tc_fence_before();

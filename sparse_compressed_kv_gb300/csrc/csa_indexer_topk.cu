@@ -35,7 +35,10 @@
 // Warp roles: 0 TMA producer, 1 TMEM allocator + tcgen05.mma issuer, 2..5
 // epilogue (one TMEM lane quarter each), 6..7 the candidate-slot table while
 // the first tiles stream in; all eight finish the CTA's last segment and run
-// the resolve.  No CTA waits for another: the hand-off is the ticket.
+// the resolve.  No CTA waits for another: the hand-off is the ticket.  With
+// FP4 keys the block has two more warps: 8, 9 and 6, 7 expand the key tiles
+// into tensor memory (lane quarters 0..3), 6..7 also convert the queries to
+// f16, and 8..9 leave when the keys are done.
 //
 // The selection code runs once per launch, in one CTA: it is written as
 // short dependency chains (thread-contiguous runs of independent loads, one
@@ -46,12 +49,14 @@
 namespace csa {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;                      // the warps that select (0..7)
 constexpr int kThreads = 32 * kWarps;
+constexpr int kThreadsFp4 = kThreads + 64;     // FP4: warps 8, 9 expand key quarters 0, 1
 constexpr int kEpiThreads = 128;               // warps 2..5
 constexpr int kBarEpi = 1;                     // named barrier of the epilogue warps
 constexpr int kBarSlots = 2;                   // epilogue + warps 6..7: slot table ready
 constexpr int kBarAux = 3;                     // warps 6..7
+constexpr int kBarMain = 5;                    // warps 0..7 (the selection's CTA-wide barrier)
 constexpr int kStages = 4;
 constexpr int kAcc = 4;
 constexpr int kN = 64;                         // MMA N: one token's indexer heads
@@ -61,17 +66,25 @@ constexpr int kABytes = 2 * kHalfBytes;        // 32 KiB per stage
 constexpr int kBoxBytes = kBoxRows * 128;      // 4 KiB: one 32-row box of one half
 constexpr int kBBytes = 2 * kN * 128;          // 16 KiB: one token's queries
 constexpr int kStageEntries = kStages * kABytes / 8;  // resolver staging in the ring
-// FP4 keys (80-byte MXFP4 rows): a ring of raw code tiles that two converter
-// warps expand into a shorter ring of f16 tiles the MMA reads; both rings fit
-// in the bf16 ring's 128 KiB, which the resolver stages in afterwards.
+// FP4 keys (80-byte MXFP4 rows): a ring of raw code tiles in shared memory.
+// Four warps, one per TMEM lane quarter (8, 9, 6, 7), expand each tile into
+// f16 keys in tensor memory, where the MMA reads its A operand; no f16 tile
+// passes through shared memory.  The raw
+// ring and a second query buffer (the next token's, loaded ahead) fit in the
+// bf16 ring's 128 KiB, which the resolver stages in afterwards.
 constexpr int kFRow = 80;
 constexpr int kFBytes = kTileKeys * kFRow;     // 10 KiB: one raw tile
-constexpr int kFStages = 6;
-constexpr int kAStagesF = 2;
-constexpr int kScaleStages = kAStagesF + kAcc; // per-key scales, read by the epilogue
-constexpr int kConvThreads = 64;               // warps 6, 7
+constexpr int kFStages = 8;
+constexpr int kATm = 4;                        // f16 key tiles in tensor memory
+constexpr int kAColsF = kIHD / 2;              // 64 columns: one f16 key per lane
+constexpr int kScaleStages = kATm + kAcc;      // per-key scales, read by the epilogue
+constexpr int kConvThreads = 64;               // warps 6, 7: the queries' conversion
+constexpr int kExpThreads = 128;               // warps 8, 9, 6, 7: the keys' expansion
 constexpr int kBarConv = 4;                    // named barrier of the converter warps
-static_assert(kAStagesF * kABytes + kFStages * kFBytes <= kStages * kABytes, "FP4 rings");
+constexpr uint32_t kTmemColsF = 512;           // accumulators + f16 key tiles
+static_assert(kAcc * kN + kATm * kAColsF <= static_cast<int>(kTmemColsF), "FP4 tensor memory");
+static_assert(kFStages * kFBytes + kBBytes <= kStages * kABytes, "FP4 rings");
+static_assert(kFStages * kFBytes % 1024 == 0, "second query buffer: 1024-byte aligned");
 constexpr int kWarmKeys = 4 * kTileKeys;       // keys a CTA warms L2 with before its layout
 
 struct DecParams {
@@ -83,7 +96,6 @@ struct DecParams {
     float *scores;
     int64_t ld;
     int32_t *status;
-    int32_t w_vec;         // w_idx 16-byte aligned: four weights per load
     FusedTopk f;           // fused selection (f.idx == nullptr: scores only)
 };
 
@@ -105,6 +117,8 @@ struct DecSmem {
     uint64_t sfull[kScaleStages];      // FP4: a tile's key scales are written
     float fscale[kScaleStages][kTileKeys];   // FP4: 2^(E_max - 127 + s_q) per key
     float qmax[2];                     // FP4: the converter warps' max |q|
+    int32_t qsi[2];                    // FP4: s_q of the token in each query buffer
+    alignas(16) float wc[4][kNIH];     // each epilogue warp's copy of its token's weights
     uint64_t rbar;                     // the resolver's staging copies
     uint32_t rphase;
     uint32_t tmem_holder;
@@ -121,8 +135,12 @@ __device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, bool active)
     if (static_cast<int>(lane_id()) == __ffs(peers) - 1) atomicAdd(&h[bin], __popc(peers));
 }
 
+// Barrier of warps 0..7 (with FP4 keys the block has two more warps, which
+// leave after the key loop).
+__device__ __forceinline__ void main_sync() { named_bar_sync(kBarMain, kThreads); }
+
 __device__ __forceinline__ void group_sync(int bar, int nthreads) {
-    if (bar == 0) __syncthreads();
+    if (bar == 0) main_sync();
     else named_bar_sync(bar, nthreads);
 }
 
@@ -373,7 +391,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
     *reinterpret_cast<uint4 *>(gh + hb + 4) = make_uint4(0, 0, 0, 0);
 #pragma unroll 1
     for (int i = tid; i < kD2Bins + kD3Bins; i += kThreads) h[i] = 0;
-    __syncthreads();
+    main_sync();
     if (tid < nseg) {
         if (m.z) atomicOr(&S.red_or, 1u);
         atomicMax(&S.red_max, m.y);
@@ -381,7 +399,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
     // slot regions in the staging area start at even entries (16-byte copies)
     uint32_t M = 0;
     const uint32_t soff = group_scan<kWarps>((m.x + 1u) & ~1u, S.bscan, warp, 0, &M);
-    __syncthreads();
+    main_sync();
     const uint32_t maxD = S.red_max >> kD1Shift;   // every key of the token in bins >= maxD is here
     bool from_row = S.red_or != 0 || M > static_cast<uint32_t>(kStageEntries);
     int32_t *out = P.f.idx + static_cast<int64_t>(t) * P.top_k;
@@ -409,7 +427,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
         if (tid < nseg && (m.x & 1u) && CSA_CHECK(soff + m.x < kStageEntries, P.status))
             stage[soff + m.x] = kNoEntry;
         if (tid == 0) S.rphase = ph ^ 1u;
-        __syncthreads();
+        main_sync();
         from_row = S.fd < 0;   // fewer than k keys >= the bound: it proves nothing
     }
     if (!from_row) {
@@ -426,7 +444,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
             const uint32_t key = static_cast<uint32_t>(stage[i] >> 32);
             if ((key >> kD1Shift) == d1) atomicAdd(&h2[(key >> kD2Shift) & (kD2Bins - 1)], 1u);
         }
-        __syncthreads();
+        main_sync();
         {
             uint32_t v[8];
             load_bins<8>(h2, kD2Bins - 8 * (tid + 1), v);
@@ -439,7 +457,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
             const uint32_t key = static_cast<uint32_t>(stage[i] >> 32);
             if ((key >> kD2Shift) == pre) atomicAdd(&h3[key & (kD3Bins - 1)], 1u);
         }
-        __syncthreads();
+        main_sync();
         {
             uint32_t v[4];
             load_bins<4>(h3, kD3Bins - 4 * (tid + 1), v);
@@ -491,10 +509,10 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
         for (int lvl = 0; lvl < 3; ++lvl) {
             const int nb = lvl == 2 ? kD3Bins : kD1Bins;
             const int shift = lvl == 0 ? kD1Shift : (lvl == 1 ? kD2Shift : 0);
-            __syncthreads();
+            main_sync();
 #pragma unroll 1
             for (int i = tid; i < kD1Bins; i += kThreads) h[i] = 0;
-            __syncthreads();
+            main_sync();
 #pragma unroll 1
             for (int64_t b = 0; b < nv; b += kThreads) {
                 const int64_t i = b + tid;
@@ -502,7 +520,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
                 const bool in = lvl == 0 || (key >> (lvl == 1 ? kD1Shift : kD2Shift)) == prefix;
                 hist_add(h, (key >> shift) & static_cast<uint32_t>(nb - 1), i < nv && in);
             }
-            __syncthreads();
+            main_sync();
             if (lvl == 2) {
                 uint32_t v[4];
                 load_bins<4>(h, kD3Bins - 4 * (tid + 1), v);
@@ -541,7 +559,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
             }
             if (pass < 2) {
                 if (lane == 0) S.bscan[warp] = cnt;
-                __syncthreads();
+                main_sync();
                 uint32_t x = 0, all = 0;
 #pragma unroll 1
                 for (int w = 0; w < kWarps; ++w) {
@@ -554,7 +572,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
                     before = x;
                     total = all;
                 }
-                __syncthreads();
+                main_sync();
             }
         }
     }
@@ -567,7 +585,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
         reinterpret_cast<TokCounters *>(P.f.state + static_cast<int64_t>(t) * kStateWords + kD1Bins +
                                         kD2Bins)->ticket = 0;
     }
-    __syncthreads();
+    main_sync();
 }
 
 // f16 x2 from two e2m1 codes (the low nibble in the low half), exact.
@@ -592,26 +610,124 @@ __device__ __forceinline__ constexpr uint32_t idesc_f16_f32() {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// One MXFP4 key row -> TMEM lane `taddr` of an f16 key tile: elements 2j and
+// 2j + 1 in column j, the e2m1 codes of block b times 2^(E_b - E_max), exact
+// (an e2m1 value times a power of two >= 2^-24 is an f16 value; blocks more
+// than 24 binades below the key's largest are dropped: below f16's range, and
+// below 2^-24 of the key's largest term).  Returns E_max.  Warp-collective:
+// a lane with no key (valid false) stores zeros.
+__device__ __forceinline__ int fp4_expand_row_tmem(const uint8_t *row, bool valid, uint32_t taddr) {
+    uint32_t cw32[16];
+    uint32_t ev = 0;
+    if (valid) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * q4);
+            cw32[4 * q4 + 0] = v.x;
+            cw32[4 * q4 + 1] = v.y;
+            cw32[4 * q4 + 2] = v.z;
+            cw32[4 * q4 + 3] = v.w;
+        }
+        ev = *reinterpret_cast<const uint32_t *>(row + 64);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) cw32[j] = 0u;
+    }
+    int eb[4];
+    int emax = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        eb[b] = static_cast<int>((ev >> (8 * b)) & 0xFFu);
+        emax = eb[b] > emax ? eb[b] : emax;
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        // block b = words 4b .. 4b + 3 = columns 16b .. 16b + 15; 2^-dlt as an
+        // f16 pair: normal down to 2^-14, subnormal to 2^-24
+        const int dlt = emax - eb[b];
+        const uint32_t hb = dlt <= 14 ? static_cast<uint32_t>(15 - dlt) << 10
+                                      : (dlt <= 24 ? 1u << (24 - dlt) : 0u);
+        const uint32_t sc = hb | (hb << 16);
+        uint32_t o[16];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t wd = cw32[4 * b + jj];   // elements 8j .. 8j + 7, j = 4b + jj
+            o[4 * jj + 0] = hmul2_bits(e2m1x2_to_f16x2(wd), sc);
+            o[4 * jj + 1] = hmul2_bits(e2m1x2_to_f16x2(wd >> 8), sc);
+            o[4 * jj + 2] = hmul2_bits(e2m1x2_to_f16x2(wd >> 16), sc);
+            o[4 * jj + 3] = hmul2_bits(e2m1x2_to_f16x2(wd >> 24), sc);
+        }
+        tmem_st16(taddr + 16u * b, o);
+    }
+    return emax;
+}
+
+// 2^(emax - 127 + qs) as an f32 (2^-127, the one subnormal case, when both are 0)
+__device__ __forceinline__ float fp4_key_scale(int emax, int qs) {
+    return emax + qs >= 1 ? __int_as_float((emax + qs) << 23) : __int_as_float(1 << 22);
+}
+
+// The barriers of the FP4 key pipeline.
+struct Fp4Bars {
+    uint64_t *f_full, *f_empty;    // raw tile landed / read by the four expander warps
+    uint64_t *a_full, *a_empty;    // f16 tile in TMEM / the MMA is done with it
+    uint64_t *sfull;               // the tile's key scales are written
+};
+
+// One expander warp's part of FP4 key tile `it`: lane l expands key
+// r = 32 * (warp's quarter) + l into TMEM lane r of key stage it % kATm and
+// writes the key's scale 2^(E_max - 127 + s_q) for the epilogue.
+__device__ __forceinline__ void fp4_expand_quarter(DecSmem &S, const uint8_t *sF, const Fp4Bars &B,
+                                                   uint32_t tmem_base, int quarter, const Tile &tl,
+                                                   int64_t row0, int64_t total_rows, int it, int qs,
+                                                   bool &dead, int32_t *status) {
+    const int lane = static_cast<int>(lane_id());
+    const int fs = it % kFStages, as = it % kATm, ss = it % kScaleStages;
+    bool ok = dead || mbar_wait(&B.f_full[fs], static_cast<uint32_t>(it / kFStages) & 1u, status);
+    ok = ok && (dead || mbar_wait(&B.a_empty[as], (static_cast<uint32_t>(it / kATm) & 1u) ^ 1u, status));
+    if (!__all_sync(0xffffffffu, ok)) dead = true;
+    tc_fence_after();
+    // the rows the producer copied: the tile's, clamped at the cache's end
+    int64_t nload = static_cast<int64_t>(tl.nunits) * kBoxRows;
+    if (row0 + nload > total_rows) nload = total_rows - row0;
+    const int r = quarter * 32 + lane;
+    const bool valid = r < nload;
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           static_cast<uint32_t>(kAcc * kN + as * kAColsF);
+    const int emax = fp4_expand_row_tmem(sF + fs * kFBytes + r * kFRow, valid, taddr);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&B.a_full[as]);
+    mbar_arrive(&B.f_empty[fs]);
+    S.fscale[ss][r] = valid ? fp4_key_scale(emax, qs) : 0.f;   // others: never scored
+    mbar_arrive(&B.sfull[ss]);
+}
+
 template <bool kFused, bool kFp4>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreads, 1)
     dec_indexer_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_q, const DecParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem<1024>(smem_raw);
-    constexpr int kAst = kFp4 ? kAStagesF : kStages;   // stages of the MMA's A ring
+    constexpr int kAst = kFp4 ? kATm : kStages;        // stages of the MMA's A operand
+    constexpr int kQb = kFp4 ? 2 : 1;                  // query buffers
     uint8_t *sA = smem;
-    uint8_t *sF = smem + kAStagesF * kABytes;          // FP4: raw code ring
+    uint8_t *sF = smem;                                // FP4: raw code ring
     uint8_t *sB = smem + kStages * kABytes;
+    uint8_t *sB1 = smem + kFStages * kFBytes;          // FP4: the second query buffer
     DecSmem &S = *reinterpret_cast<DecSmem *>(sB + kBBytes);
     uint64_t *a_full = S.bars;
     uint64_t *a_empty = a_full + kAst;
-    uint64_t *b_full = a_empty + kAst;
-    uint64_t *b_empty = b_full + 1;
-    uint64_t *acc_full = b_full + 2;
+    uint64_t *b_full = a_empty + kAst;                 // [kQb]
+    uint64_t *b_empty = b_full + kQb;                  // [kQb]
+    uint64_t *acc_full = b_empty + kQb;
     uint64_t *acc_empty = acc_full + kAcc;
-    uint64_t *b_conv = acc_empty + kAcc;               // FP4: q converted to f16
-    uint64_t *f_full = b_conv + 1;                     // FP4: raw tile landed
-    uint64_t *f_empty = f_full + kFStages;             // FP4: raw tile converted
+    uint64_t *b_conv = acc_empty + kAcc;               // FP4 [2]: q converted to f16
+    uint64_t *f_full = b_conv + 2;                     // FP4: raw tile landed
+    uint64_t *f_empty = f_full + kFStages;             // FP4: raw tile expanded
+    static_assert(2 * kATm + 4 + 2 * kAcc + 2 + 2 * kFStages <= 40 && 2 * kStages + 2 + 2 * kAcc <= 40,
+                  "pipeline barriers");
+    const Fp4Bars fb{f_full, f_empty, a_full, a_empty, S.sfull};
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -622,22 +738,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kAst; ++s) {
-            mbar_init(&a_full[s], kFp4 ? kConvThreads : 1);
+            mbar_init(&a_full[s], kFp4 ? kExpThreads : 1);
             mbar_init(&a_empty[s], 1);
         }
-        mbar_init(b_full, 1);
-        mbar_init(b_empty, 1);
+        for (int s = 0; s < kQb; ++s) {
+            mbar_init(&b_full[s], 1);
+            mbar_init(&b_empty[s], 1);
+        }
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], kEpiThreads);
         }
         if (kFp4) {
-            mbar_init(b_conv, kConvThreads);
+            for (int s = 0; s < 2; ++s) mbar_init(&b_conv[s], kConvThreads);
             for (int s = 0; s < kFStages; ++s) {
                 mbar_init(&f_full[s], 1);
-                mbar_init(&f_empty[s], kConvThreads);
+                mbar_init(&f_empty[s], kExpThreads);
             }
-            for (int s = 0; s < kScaleStages; ++s) mbar_init(&S.sfull[s], kConvThreads);
+            for (int s = 0; s < kScaleStages; ++s) mbar_init(&S.sfull[s], kExpThreads);
         }
         mbar_init(&S.rbar, 1);
         mbar_fence_init();
@@ -647,11 +765,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         S.rphase = 0;
     }
     if (warp == 1) {
-        tmem_alloc(&S.tmem_holder, kAcc * kN);
+        tmem_alloc(&S.tmem_holder, kFp4 ? kTmemColsF : static_cast<uint32_t>(kAcc * kN));
         tmem_relinquish();
     }
+    constexpr int kCta = kFp4 ? kThreadsFp4 : kThreads;
     if (kFused)
-        for (int i = tid; i < kD1Bins; i += kThreads) S.hist[i] = 0;
+        for (int i = tid; i < kD1Bins; i += kCta) S.hist[i] = 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -681,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- every token's visible blocks and units (the same in every CTA)
-    for (int t = tid; t < T; t += kThreads) {
+    for (int t = tid; t < T; t += kCta) {
         const TokenView v = token_view(P.L, P.ratio, t);
         if (v.bad && c == 0) raise_status(P.status, v.bad);
         const int64_t nv = v.bad & CSA_DEV_BAD_LAYOUT ? 0 : v.n_vis;
@@ -701,6 +820,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
 
     if (warp == 0) {
+      if constexpr (kFp4) {
+        // ------------------------------------------------ FP4: TMA / bulk producer
+        // Each token's queries go to buffer g & 1 (g counts the CTA's
+        // tokens) once the MMA is done with token g - 2's; the raw key tiles
+        // fill the ring behind them.
+        if (lane == 0 && ua < ub) {
+            const uint64_t pol_k = policy_evict_first();
+            const uint64_t pol_q = policy_evict_last();
+            int t = token_of(S.U, T, ua), cur = -1, g = -1;
+            int64_t u = ua;
+            int it = 0;
+            bool dead = false;
+            Tile tl;
+            while (next_tile(S.U, ub, t, u, tl)) {
+                if (tl.t != cur) {
+                    ++g;
+                    const int slot = g & 1;
+                    const uint32_t ph = static_cast<uint32_t>(g >> 1) & 1u;
+                    if (!dead && !mbar_wait(&b_empty[slot], ph ^ 1u, P.status)) dead = true;
+                    uint8_t *dst = slot ? sB1 : sB;
+                    mbar_arrive_expect_tx(&b_full[slot], kBBytes);
+                    tma_load_2d(dst, &tm_q, 0, tl.t * kN, &b_full[slot], pol_q);
+                    tma_load_2d(dst + kBBytes / 2, &tm_q, 64, tl.t * kN, &b_full[slot], pol_q);
+                    cur = tl.t;
+                }
+                // the tile's rows are contiguous: one bulk copy (clamped at the
+                // cache's end; rows past it are never scored)
+                const int fs = it % kFStages;
+                const uint32_t ph = static_cast<uint32_t>(it / kFStages) & 1u;
+                if (!dead && !mbar_wait(&f_empty[fs], ph ^ 1u, P.status)) dead = true;
+                const int64_t r0 = S.off[tl.t] + tl.s0;
+                int64_t nr = static_cast<int64_t>(tl.nunits) * kBoxRows;
+                if (r0 + nr > P.L.total_comp_rows) nr = P.L.total_comp_rows - r0;
+                const uint32_t bytes = static_cast<uint32_t>(nr * kFRow);
+                mbar_arrive_expect_tx(&f_full[fs], bytes);
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+                    "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(sF + fs * kFBytes)),
+                    "l"(P.k_idx + r0 * kFRow), "r"(bytes), "r"(smem_addr(&f_full[fs])), "l"(pol_k)
+                    : "memory");
+                ++it;
+            }
+        }
+      } else {
         // ------------------------------------------------ TMA producer
         if (lane == 0 && ua < ub) {
             const uint64_t pol_k = policy_evict_first();
@@ -722,44 +885,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cur = tl.t;
                     ++gsw;
                 }
-                if constexpr (kFp4) {
-                    // the tile's rows are contiguous: one bulk copy (clamped at
-                    // the cache's end; rows past it are never scored)
-                    const int fs = it % kFStages;
-                    const uint32_t ph = static_cast<uint32_t>(it / kFStages) & 1u;
-                    if (!dead && !mbar_wait(&f_empty[fs], ph ^ 1u, P.status)) dead = true;
-                    const int64_t r0 = row_base + tl.s0;
-                    int64_t nr = static_cast<int64_t>(tl.nunits) * kBoxRows;
-                    if (r0 + nr > P.L.total_comp_rows) nr = P.L.total_comp_rows - r0;
-                    const uint32_t bytes = static_cast<uint32_t>(nr * kFRow);
-                    mbar_arrive_expect_tx(&f_full[fs], bytes);
-                    asm volatile(
-                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-                        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(sF + fs * kFBytes)),
-                        "l"(P.k_idx + r0 * kFRow), "r"(bytes), "r"(smem_addr(&f_full[fs])), "l"(pol_k)
-                        : "memory");
-                } else {
-                    const int stage = it % kStages;
-                    const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-                    if (!dead && !mbar_wait(&a_empty[stage], ph ^ 1u, P.status)) dead = true;
-                    mbar_arrive_expect_tx(&a_full[stage], static_cast<uint32_t>(tl.nunits) * 2u * kBoxBytes);
-                    uint8_t *dst = sA + stage * kABytes;
-                    const int32_t row0 = static_cast<int32_t>(row_base + tl.s0);
-                    for (int bx = 0; bx < tl.nunits; ++bx) {
-                        tma_load_2d(dst + bx * kBoxBytes, &tm_k, 0, row0 + bx * kBoxRows, &a_full[stage],
-                                    pol_k);
-                        tma_load_2d(dst + kHalfBytes + bx * kBoxBytes, &tm_k, 64, row0 + bx * kBoxRows,
-                                    &a_full[stage], pol_k);
-                    }
+                const int stage = it % kStages;
+                const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+                if (!dead && !mbar_wait(&a_empty[stage], ph ^ 1u, P.status)) dead = true;
+                mbar_arrive_expect_tx(&a_full[stage], static_cast<uint32_t>(tl.nunits) * 2u * kBoxBytes);
+                uint8_t *dst = sA + stage * kABytes;
+                const int32_t row0 = static_cast<int32_t>(row_base + tl.s0);
+                for (int bx = 0; bx < tl.nunits; ++bx) {
+                    tma_load_2d(dst + bx * kBoxBytes, &tm_k, 0, row0 + bx * kBoxRows, &a_full[stage], pol_k);
+                    tma_load_2d(dst + kHalfBytes + bx * kBoxBytes, &tm_k, 64, row0 + bx * kBoxRows,
+                                &a_full[stage], pol_k);
                 }
                 ++it;
             }
         }
+      }
     } else if (warp == 1) {
+      if constexpr (kFp4) {
+        // ------------------------------------------------ FP4: MMA issuer (A from tensor memory)
+        if (lane == 0 && ua < ub) {
+            constexpr uint32_t idesc = idesc_f16_f32<kTileKeys, kN>();
+            int t = token_of(S.U, T, ua), cur = -1, g = -1;
+            int64_t u = ua;
+            int it = 0;
+            bool dead = false;
+            Tile tl;
+            while (next_tile(S.U, ub, t, u, tl)) {
+                if (tl.t != cur) {
+                    ++g;   // the token's queries, converted to f16
+                    if (!dead && !mbar_wait(&b_conv[g & 1], static_cast<uint32_t>(g >> 1) & 1u, P.status))
+                        dead = true;
+                    cur = tl.t;
+                }
+                const int acc = it % kAcc;
+                if (!dead && !mbar_wait(&acc_empty[acc], (static_cast<uint32_t>(it / kAcc) & 1u) ^ 1u,
+                                        P.status))
+                    dead = true;
+                const int stage = it % kATm;
+                if (!dead && !mbar_wait(&a_full[stage], static_cast<uint32_t>(it / kATm) & 1u, P.status))
+                    dead = true;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kN);
+                const uint32_t a_tm = tmem_base + static_cast<uint32_t>(kAcc * kN + stage * kAColsF);
+                const uint32_t b_base = smem_addr((g & 1) ? sB1 : sB);
+#pragma unroll
+                for (int kk = 0; kk < kIHD / 16; ++kk) {
+                    const uint32_t b_addr = b_base + (kk >> 2) * (kBBytes / 2) + (kk & 3) * 32;
+                    umma_f16_ts(d_tmem, a_tm + static_cast<uint32_t>(kk * 8), sw128_kmajor_desc(b_addr), idesc,
+                                kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&a_empty[stage]);
+                umma_commit(&acc_full[acc]);
+                if (tl.last) umma_commit(&b_empty[g & 1]);
+                ++it;
+            }
+        }
+      } else {
         // ------------------------------------------------ MMA issuer
         if (lane == 0 && ua < ub) {
-            constexpr uint32_t idesc =
-                kFp4 ? idesc_f16_f32<kTileKeys, kN>() : idesc_bf16_f32<kTileKeys, kN>();
+            constexpr uint32_t idesc = idesc_bf16_f32<kTileKeys, kN>();
             int t = token_of(S.U, T, ua), cur = -1;
             int64_t u = ua;
             uint32_t gsw = 0;
@@ -770,8 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Tile tl;
             while (next_tile(S.U, ub, t, u, tl)) {
                 if (tl.t != cur) {
-                    // FP4: the converter warps turn the token's q into f16 first
-                    if (!dead && !mbar_wait(kFp4 ? b_conv : b_full, gsw & 1u, P.status)) dead = true;
+                    if (!dead && !mbar_wait(b_full, gsw & 1u, P.status)) dead = true;
                     cur = tl.t;
                     ++gsw;
                 }
@@ -779,8 +962,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!dead && !mbar_wait(&acc_empty[acc], (static_cast<uint32_t>(it / kAcc) & 1u) ^ 1u,
                                         P.status))
                     dead = true;
-                const int stage = it % kAst;
-                const uint32_t ph = static_cast<uint32_t>(it / kAst) & 1u;
+                const int stage = it % kStages;
+                const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
                 if (!dead && !mbar_wait(&a_full[stage], ph, P.status)) dead = true;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kN);
@@ -798,6 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++it;
             }
         }
+      }
     } else if (warp < 6) {
         // ------------------------------------------------ epilogue
         // No early exit from this loop: segment ends meet at named barriers,
@@ -810,8 +994,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t u = ua, seg_u0 = ua;
         int it = 0;
         bool dead = false, slots_ready = false;
+        int wcur = -1;
+        float *wc = S.wc[warp - 2];
         Tile tl;
         while (next_tile(S.U, ub, t, u, tl)) {
+            if (tl.t != wcur) {
+                // the token's 64 weights, once per token, for broadcast reads
+                const float *wt = P.w_idx + static_cast<int64_t>(tl.t) * kNIH;
+                __syncwarp();
+                wc[lane] = __ldg(wt + lane);
+                wc[lane + 32] = __ldg(wt + lane + 32);
+                __syncwarp();
+                wcur = tl.t;
+            }
             const int acc = it % kAcc;
             bool ok = dead || mbar_wait(&acc_full[acc], static_cast<uint32_t>(it / kAcc) & 1u, P.status);
             if (!__all_sync(0xffffffffu, ok)) dead = true;
@@ -838,27 +1033,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t nv = S.nvis[tk];
             const int64_t s = tl.s0 + row;
             const bool valid = row < tl.nunits * kBoxRows && s < nv;
-            const float *wt = P.w_idx + static_cast<int64_t>(tk) * kNIH;
             float part[4] = {0.f, 0.f, 0.f, 0.f};  // four short chains, summed in order
-            if (P.w_vec) {
-                const float4 *wt4 = reinterpret_cast<const float4 *>(wt);
+            const float4 *wc4 = reinterpret_cast<const float4 *>(wc);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
+            for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-                    for (int i = 0; i < 16; i += 4) {
-                        const float4 w4 = __ldg(wt4 + (c4 * 16 + i) / 4);
-                        part[c4] = fmaf(w4.x, fmaxf(v[c4][i + 0], 0.f), part[c4]);
-                        part[c4] = fmaf(w4.y, fmaxf(v[c4][i + 1], 0.f), part[c4]);
-                        part[c4] = fmaf(w4.z, fmaxf(v[c4][i + 2], 0.f), part[c4]);
-                        part[c4] = fmaf(w4.w, fmaxf(v[c4][i + 3], 0.f), part[c4]);
-                    }
-            } else {
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        part[c4] = fmaf(__ldg(wt + c4 * 16 + i), fmaxf(v[c4][i], 0.f), part[c4]);
-            }
+                for (int i = 0; i < 16; i += 4) {
+                    const float4 w4 = wc4[(c4 * 16 + i) / 4];
+                    part[c4] = fmaf(w4.x, fmaxf(v[c4][i + 0], 0.f), part[c4]);
+                    part[c4] = fmaf(w4.y, fmaxf(v[c4][i + 1], 0.f), part[c4]);
+                    part[c4] = fmaf(w4.z, fmaxf(v[c4][i + 2], 0.f), part[c4]);
+                    part[c4] = fmaf(w4.w, fmaxf(v[c4][i + 3], 0.f), part[c4]);
+                }
             // (FP4: relu(c x) = c relu(x) for the positive key scale c)
             const float score = ((part[0] + part[1]) + (part[2] + part[3])) * ksc;
             if (valid && CSA_CHECK(s < P.ld, P.status)) P.scores[static_cast<int64_t>(tk) * P.ld + s] = score;
@@ -883,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++it;
         }
         if (kFused && !slots_ready) named_bar_sync(kBarSlots, kEpiThreads + 64);
-    } else {
+    } else if (warp < kWarps) {
       if constexpr (kFused) {
         // ------------------------------------------------ slot table (warps 6, 7)
         // candidate slots: one per (token, CTA that owns part of it)
@@ -909,30 +1095,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_arrive(kBarSlots, kEpiThreads + 64);
       }
       if constexpr (kFp4) {
-        // ------------------------------------------------ FP4 converters (warps 6, 7)
-        // The token's q: bf16 -> f16 in place, scaled by 2^-s_q so that it
-        // stays below f16's largest value.  A key tile: the e2m1 codes of
-        // each block b scaled by 2^(E_b - E_max) in f16 (exact: an e2m1 value
-        // times a power of two >= 2^-24 is an f16 value; blocks more than 24
-        // binades below the key's largest contribute below f16's range and
-        // are dropped), laid out as the bf16 tiles are (128-byte swizzle,
-        // K-major); the per-key factor 2^(E_max - 127 + s_q) goes to the
-        // epilogue.
+        // ------------------------------------------------ FP4: queries + expansion of TMEM lanes 64..127
+        // Each token's q: bf16 -> f16 in place, scaled by 2^-s_q so that it
+        // stays below f16's largest value (s_q goes to the other expanders).
+        // Then these warps expand their quarters of each key tile, as warps
+        // 0 and 1 do theirs.
         const int ct = tid - 192;
         const int cw = warp - 6;
-        int t = ua < ub ? token_of(S.U, T, ua) : 0, cur = -1;
+        int t = ua < ub ? token_of(S.U, T, ua) : 0, cur = -1, g = -1;
         int64_t u = ua;
-        uint32_t gsw = 0;
         int it = 0;
         bool dead = false;
         int qs = 0;
         Tile tl;
         while (next_tile(S.U, ub, t, u, tl)) {
             if (tl.t != cur) {
-                const bool ok = dead || mbar_wait(b_full, gsw & 1u, P.status);
+                ++g;
+                uint8_t *qb = (g & 1) ? sB1 : sB;
+                const bool ok = dead || mbar_wait(&b_full[g & 1], static_cast<uint32_t>(g >> 1) & 1u, P.status);
                 if (!__all_sync(0xffffffffu, ok)) dead = true;
-                uint4 *qv = reinterpret_cast<uint4 *>(sB) + ct * (kBBytes / 16 / kConvThreads);
                 constexpr int kQv = kBBytes / 16 / kConvThreads;   // 16 x 16 bytes per thread
+                uint4 *qv = reinterpret_cast<uint4 *>(qb) + ct * kQv;
                 uint4 w[kQv];
                 float mx = 0.f;
 #pragma unroll
@@ -964,78 +1147,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     qv[j] = make_uint4(o[0], o[1], o[2], o[3]);
                 }
+                if (ct == 0) S.qsi[g & 1] = qs;
                 named_bar_sync(kBarConv, kConvThreads);   // S.qmax is read by both warps first
                 fence_proxy_async_smem();
-                mbar_arrive(b_conv);
+                mbar_arrive(&b_conv[g & 1]);
                 cur = tl.t;
-                ++gsw;
             }
-            const int fs = it % kFStages;
-            const int as = it % kAStagesF;
-            const int ss = it % kScaleStages;
-            bool ok = dead || mbar_wait(&f_full[fs], static_cast<uint32_t>(it / kFStages) & 1u, P.status);
-            ok = ok && (dead || mbar_wait(&a_empty[as], (static_cast<uint32_t>(it / kAStagesF) & 1u) ^ 1u,
-                                          P.status));
-            if (!__all_sync(0xffffffffu, ok)) dead = true;
-            const int nrows = tl.nunits * kBoxRows;
-            const uint8_t *fa = sF + fs * kFBytes;
-            uint8_t *dA = sA + as * kABytes;
-            for (int r = ct; r < kTileKeys; r += kConvThreads) {
-                if (r >= nrows) {
-                    S.fscale[ss][r] = 0.f;   // not a key of this tile: never scored
-                    continue;
-                }
-                const uint8_t *row = fa + r * kFRow;
-                uint32_t cw32[16];
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * q4);
-                    cw32[4 * q4 + 0] = v.x;
-                    cw32[4 * q4 + 1] = v.y;
-                    cw32[4 * q4 + 2] = v.z;
-                    cw32[4 * q4 + 3] = v.w;
-                }
-                const uint32_t ev = *reinterpret_cast<const uint32_t *>(row + 64);
-                int eb[4];
-                int emax = 0;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    eb[b] = static_cast<int>((ev >> (8 * b)) & 0xFFu);
-                    emax = eb[b] > emax ? eb[b] : emax;
-                }
-                // 2^-dlt as an f16 pair: normal down to 2^-14, subnormal to 2^-24
-                uint32_t scb[4];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int dlt = emax - eb[b];
-                    const uint32_t hb = dlt <= 14 ? static_cast<uint32_t>(15 - dlt) << 10
-                                                  : (dlt <= 24 ? 1u << (24 - dlt) : 0u);
-                    scb[b] = hb | (hb << 16);
-                }
-                // 2^(emax - 127 + qs) as an f32 (2^-127, the one subnormal case, when both are 0)
-                S.fscale[ss][r] =
-                    emax + qs >= 1 ? __int_as_float((emax + qs) << 23) : __int_as_float(1 << 22);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    // elements 8j .. 8j + 7 (code bytes 4j .. 4j + 3) of block j / 4
-                    const uint32_t wd = cw32[j];
-                    const uint32_t sc = scb[j >> 2];
-                    const uint32_t o0 = hmul2_bits(e2m1x2_to_f16x2(wd), sc);
-                    const uint32_t o1 = hmul2_bits(e2m1x2_to_f16x2(wd >> 8), sc);
-                    const uint32_t o2 = hmul2_bits(e2m1x2_to_f16x2(wd >> 16), sc);
-                    const uint32_t o3 = hmul2_bits(e2m1x2_to_f16x2(wd >> 24), sc);
-                    const int hh = j >> 3, c8 = j & 7;
-                    *reinterpret_cast<uint4 *>(dA + hh * kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) =
-                        make_uint4(o0, o1, o2, o3);
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&a_full[as]);
-            mbar_arrive(&f_empty[fs]);
-            mbar_arrive(&S.sfull[ss]);
+            fp4_expand_quarter(S, sF, fb, tmem_base, warp & 3, tl, S.off[tl.t] + tl.s0, P.L.total_comp_rows, it,
+                               qs, dead, P.status);
             ++it;
         }
       }
+    }
+    if constexpr (kFp4) {
+        if (warp >= kWarps) {
+            // ------------------------------------------------ FP4: expansion of TMEM lanes 0..63 (warps 8, 9)
+            int t = ua < ub ? token_of(S.U, T, ua) : 0, cur = -1, g = -1;
+            int64_t u = ua;
+            int it = 0;
+            bool dead = false;
+            int qs = 0;
+            Tile tl;
+            while (next_tile(S.U, ub, t, u, tl)) {
+                if (tl.t != cur) {
+                    ++g;   // the token's s_q, from the converter warps
+                    const bool okq = dead || mbar_wait(&b_conv[g & 1], static_cast<uint32_t>(g >> 1) & 1u,
+                                                       P.status);
+                    if (!__all_sync(0xffffffffu, okq)) dead = true;
+                    qs = S.qsi[g & 1];
+                    cur = tl.t;
+                }
+                fp4_expand_quarter(S, sF, fb, tmem_base, warp & 3, tl, S.off[tl.t] + tl.s0,
+                                   P.L.total_comp_rows, it, qs, dead, P.status);
+                ++it;
+            }
+            // done: every TMEM store of these warps completed before the
+            // MMAs that read it, and the rest of the kernel is warps 0..7's
+            return;
+        }
     }
 
     if (kFused && ua < ub) {
@@ -1045,10 +1194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         finalize_segment<kWarps>(P, S, tk, su0, ub, ua, K32, Ge, c, tid, 0);
     }
     tc_fence_before();
-    __syncthreads();
+    main_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kAcc * kN);
+        tmem_dealloc(tmem_base, kFp4 ? kTmemColsF : static_cast<uint32_t>(kAcc * kN));
     }
     if (kFused) {
         const int nr = S.nresolve;
@@ -1057,7 +1206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-size_t dec_smem_bytes() { return 1024 + kStages * kABytes + kBBytes + sizeof(DecSmem); }
+constexpr size_t kDecSmemBytes = 1024 + kStages * kABytes + kBBytes + sizeof(DecSmem);
+static_assert(kDecSmemBytes <= 227 * 1024, "decode indexer shared memory");
+
+size_t dec_smem_bytes() { return kDecSmemBytes; }
 
 int dec_grid(const csa_layout_t &L, int sm_count) {
     const int64_t units = static_cast<int64_t>(L.num_tokens) *
@@ -1109,7 +1261,6 @@ cudaError_t launch_decode_indexer(const Launch &lc, const csa_layout_t &L, const
     P.scores = scores;
     P.ld = ld;
     P.status = status;
-    P.w_vec = reinterpret_cast<uintptr_t>(w_idx) % 16 == 0 ? 1 : 0;
     P.f = fused ? *fused : FusedTopk{};
     const size_t smem = dec_smem_bytes();
     const int grid = dec_grid(L, lc.sm_count);
@@ -1117,7 +1268,7 @@ cudaError_t launch_decode_indexer(const Launch &lc, const csa_layout_t &L, const
                       : (fp4 ? dec_indexer_kernel<false, true> : dec_indexer_kernel<false, false>);
     cudaError_t e = set_kernel_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, lc.stream, tk, tq, P);
+    return launch_pdl(kern, dim3(grid), dim3(fp4 ? kThreadsFp4 : kThreads), smem, lc.stream, tk, tq, P);
 }
 
 }  // namespace csa
