@@ -421,6 +421,20 @@ def decode_only_leg(args, device):
         def step(i):
             d, lay, prm, out = runs[i % 2]
             csa.csa_hca_decode(lay, prm, d.comp_kv, d.q, out, status, ws, stream=stream)
+    elif name == "fp4":
+        # the 1m workload with its keys quantized to MXFP4 once, before the steps
+        layers = make_layers("1m", 2, device, csa, seed0=0)
+        ws = csa.workspace(layers[0].layout, layers[0].prm)
+        rows = []
+        for L in layers:
+            r = torch.empty(L.wl.k_idx.shape[0], csa.FP4_ROW, dtype=torch.uint8, device=device)
+            csa.csa_fp4_quantize_keys(L.d.k_idx, r, stream=stream)
+            rows.append(r)
+
+        def step(i):
+            L = layers[i % 2]
+            csa.csa_decode_fp4(L.layout, L.prm, L.d.q_idx, L.d.w_idx, rows[i % 2], L.d.comp_kv, L.d.q,
+                               L.out, status, ws, idx_out=L.idx, stream=stream)
     else:
         layers = make_layers(name, 2, device, csa, seed0=0 if name == "1m" else 77)
         ws = csa.workspace(layers[0].layout, layers[0].prm)
@@ -852,7 +866,7 @@ def main():
     ap.add_argument("--prefill-tokens", type=int, default=4096)
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill-indexer leg and print its object (for profiling)")
-    ap.add_argument("--decode-only", choices=["1m", "batch32", "hca1m"], default=None,
+    ap.add_argument("--decode-only", choices=["1m", "batch32", "hca1m", "fp4"], default=None,
                     help="run only eager decode steps of this workload (2 rotating layers) and "
                          "print their mean time (for profiling)")
     args = ap.parse_args()
