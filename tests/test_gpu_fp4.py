@@ -116,3 +116,31 @@ def test_fp4_decode_1m(cuda_device):
     common = len(set(bidx.cpu().numpy()[0].tolist()) & set(fidx.cpu().numpy()[0].tolist()))
     print(f"fp4 vs bf16 selection overlap at 1M: {common}/{wl.top_k}")
     assert run.dev_status() == 0
+
+
+@pytest.mark.parametrize("top_k", [8, 16])
+def test_fp4_many_tokens_per_cta(cuda_device, top_k):
+    # ~500 short sequences of 1..3 key units each: every CTA's range crosses
+    # several token boundaries, so each token's queries are loaded and
+    # converted ahead into alternating buffers (first, second and reused
+    # buffers); tokens with no more visible blocks than top_k take the
+    # select-everything path between them
+    rng = np.random.default_rng(17)
+    B = 480
+    n_comp = rng.integers(5, 97, B).tolist()
+    seq_lens = [4 * n + int(rng.integers(0, 4)) for n in n_comp]
+    wl = W.make("fp4_many", seed=18, seq_lens=seq_lens, tokens=[1] * B, n_comp=n_comp,
+                top_k=top_k, n_heads=16, swa_cap=128)
+    run = H.Run(wl, cuda_device)
+    rows = gpu_rows(run.d.k_idx)
+    sc = fp4_scores(run, rows)
+    H.check_scores(dequantized(wl), sc)
+    idx, n_sel = run.topk(sc)
+    H.check_topk_exact(wl, sc, idx, n_sel)
+    out, fidx = fp4_decode(run, rows)
+    torch.cuda.synchronize()
+    assert torch.equal(fidx, idx)
+    toks = list(range(0, B, 37))
+    kv_buf, kv_len = H.gpu_rows(run, idx, n_sel)
+    H.check_attention(wl, kv_buf, kv_len, out, tokens=toks)
+    assert run.dev_status() == 0
