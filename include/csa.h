@@ -57,7 +57,7 @@ extern "C" {
 typedef enum {
     CSA_OK = 0,
     CSA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misaligned buffer */
-    CSA_ERR_UNSUPPORTED = 2,      /* dims or device this build does not handle */
+    CSA_ERR_UNSUPPORTED = 2,      /* dims or device the library does not handle */
     CSA_ERR_CAPACITY = 3,         /* a buffer is smaller than the layout needs */
     CSA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
     CSA_ERR_DEVICE_FAULT = 5,     /* reserved: a device-status bit was read back */
@@ -90,7 +90,7 @@ typedef struct {
     const int64_t *swa_first_pos;   /* [B] oldest position the ring still holds */
 } csa_layout_t;
 
-/* Problem constants.  This build supports n_ih = 64, ihd = 128, hd = 512,
+/* Problem constants.  The library supports n_ih = 64, ihd = 128, hd = 512,
  * n_heads a multiple of 16 up to 128, 1 <= top_k <= 2048, window <= swa_cap. */
 typedef struct {
     int32_t n_ih;     /* indexer heads (64) */

@@ -12,7 +12,7 @@
 
 namespace csa {
 
-// Problem constants this build supports.
+// Problem constants the library supports.
 constexpr int kNIH = 64;        // indexer heads
 constexpr int kIHD = 128;       // indexer key width
 constexpr int kHD = 512;        // main row width (shared key/value)
