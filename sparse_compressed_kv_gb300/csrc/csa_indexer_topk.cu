@@ -662,9 +662,14 @@ __device__ __forceinline__ int fp4_expand_row_tmem(const uint8_t *row, bool vali
     return emax;
 }
 
-// 2^(emax - 127 + qs) as an f32 (2^-127, the one subnormal case, when both are 0)
+// 2^(emax - 127 + qs) as an f32, built from its bits: normal, subnormal,
+// zero below f32's range, infinity above it (where the product overflows)
 __device__ __forceinline__ float fp4_key_scale(int emax, int qs) {
-    return emax + qs >= 1 ? __int_as_float((emax + qs) << 23) : __int_as_float(1 << 22);
+    const int e = emax - 127 + qs;
+    if (e > 127) return __int_as_float(0x7F800000);
+    if (e >= -126) return __int_as_float((e + 127) << 23);
+    if (e >= -149) return __int_as_float(1 << (e + 149));
+    return 0.f;
 }
 
 // The barriers of the FP4 key pipeline.
@@ -1096,8 +1101,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreads, 1)
       }
       if constexpr (kFp4) {
         // ------------------------------------------------ FP4: queries + expansion of TMEM lanes 64..127
-        // Each token's q: bf16 -> f16 in place, scaled by 2^-s_q so that it
-        // stays below f16's largest value (s_q goes to the other expanders).
+        // Each token's q: bf16 -> f16 in place, scaled by 2^-s_q so that its
+        // largest magnitude lands in [2^14, 2^15): below f16's largest value
+        // and clear of its subnormals (s_q goes to the other expanders).
         // Then these warps expand their quarters of each key tile, as warps
         // 0 and 1 do theirs.
         const int ct = tid - 192;
@@ -1133,7 +1139,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreads, 1)
                 if (lane == 0) S.qmax[cw] = mx;
                 named_bar_sync(kBarConv, kConvThreads);
                 mx = fmaxf(S.qmax[0], S.qmax[1]);
-                qs = mx >= 32768.f ? ilogbf(mx) - 14 : 0;
+                // (|s_q| <= 126 keeps 2^-s_q a finite f32; all-zero q: s_q = 0)
+                qs = mx > 0.f ? min(max(ilogbf(mx) - 14, -126), 126) : 0;
                 const float f = ldexpf(1.f, -qs);
 #pragma unroll
                 for (int j = 0; j < kQv; ++j) {

@@ -144,3 +144,19 @@ def test_fp4_many_tokens_per_cta(cuda_device, top_k):
     kv_buf, kv_len = H.gpu_rows(run, idx, n_sel)
     H.check_attention(wl, kv_buf, kv_len, out, tokens=toks)
     assert run.dev_status() == 0
+
+
+@pytest.mark.parametrize("q_exp", [-20, 20])
+def test_fp4_scores_query_scale(cuda_device, q_exp):
+    # the query scaled by an exact power of two far from 1: the f16 queries
+    # of the FP4 path must keep their precision (no f16 subnormals, no
+    # overflow), so the scores stay within the bound against the oracle
+    wl = W.tiny(seed=9)
+    scaled = (wl.q_idx.float() * 2.0 ** q_exp).to(torch.bfloat16)
+    assert torch.equal(scaled.float(), wl.q_idx.float() * 2.0 ** q_exp)   # exact in bf16
+    wl = dataclasses.replace(wl, q_idx=scaled)
+    run = H.Run(wl, cuda_device)
+    rows = gpu_rows(run.d.k_idx)
+    sc = fp4_scores(run, rows)
+    H.check_scores(dequantized(wl), sc)
+    assert run.dev_status() == 0
