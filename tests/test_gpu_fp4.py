@@ -160,3 +160,26 @@ def test_fp4_scores_query_scale(cuda_device, q_exp):
     sc = fp4_scores(run, rows)
     H.check_scores(dequantized(wl), sc)
     assert run.dev_status() == 0
+
+
+@pytest.mark.parametrize("q_exp", [0, -20])
+def test_fp4_prefill_chunk(cuda_device, q_exp):
+    # 16 query tokens of one sequence (a prefill chunk): FP4 keys go through
+    # the chunk indexer (converter warps, bf16 expansion) and the separate
+    # top-k instead of the decode kernel
+    wl = W.make("fp4_chunk", seed=23, seq_lens=[8192], tokens=[16], n_comp=[2051], top_k=64,
+                n_heads=16, swa_cap=144)
+    if q_exp:
+        wl = dataclasses.replace(wl, q_idx=(wl.q_idx.float() * 2.0 ** q_exp).to(torch.bfloat16))
+    run = H.Run(wl, cuda_device)
+    rows = gpu_rows(run.d.k_idx)
+    sc = fp4_scores(run, rows)
+    H.check_scores(dequantized(wl), sc, blocks_per_token=300)
+    idx, n_sel = run.topk(sc)
+    H.check_topk_exact(wl, sc, idx, n_sel)
+    out, fidx = fp4_decode(run, rows)
+    torch.cuda.synchronize()
+    assert torch.equal(fidx, idx)
+    kv_buf, kv_len = H.gpu_rows(run, idx, n_sel)
+    H.check_attention(wl, kv_buf, kv_len, out, tokens=[0, 7, 15])
+    assert run.dev_status() == 0
