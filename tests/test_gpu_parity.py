@@ -300,3 +300,17 @@ def test_indexer_topk_equals_topk_on_the_scores(cuda_device, name):
         # the selection is the tail of the cache (rounding may swap neighbours)
         assert idx.cpu().numpy()[0].min() >= 1800
     assert run.dev_status() == 0
+
+
+@pytest.mark.parametrize("B", [480, 700, 1100])
+def test_many_short_sequences(cuda_device, B):
+    # B sequences of 20..60 blocks, one token each: 480 keeps the selection
+    # folded into the decode indexer with several tokens per CTA, 700 is past
+    # the folded selection's token limit (decode indexer + separate top-k),
+    # 1100 past the decode indexer's (the chunk indexer, one token per tile)
+    rng = np.random.default_rng(B)
+    n_comp = rng.integers(20, 61, B).tolist()
+    seq_lens = [4 * n + int(rng.integers(0, 4)) for n in n_comp]
+    wl = W.make(f"many{B}", seed=B, seq_lens=seq_lens, tokens=[1] * B, n_comp=n_comp, top_k=16,
+                n_heads=16)
+    full_chain(H.Run(wl, cuda_device), check_recall=False)
