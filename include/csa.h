@@ -75,7 +75,15 @@ typedef enum {
 #define CSA_DEV_CHECK       0x40  /* libcsa_checks.so only: an index inside the library
                                      left its array; the access was skipped */
 
-/* Where each query token's rows live.  Device arrays unless marked (host). */
+/* Where each query token's rows live.  Device arrays unless marked (host).
+ * The library's kernels may read tok_seq, tok_pos, comp_off and
+ * swa_first_pos as soon as they start, while a preceding kernel that allows
+ * programmatic dependent launch may still run: these arrays must not be
+ * written by such a kernel (the library's own kernels never write them; a
+ * copy, or a kernel without that launch attribute, completes before the
+ * next one starts).  Everything else a call reads (queries, weights, keys,
+ * rows, the window ring) is read only after the preceding kernel has
+ * finished. */
 typedef struct {
     int32_t num_seqs;               /* (host) B >= 1 */
     int32_t num_tokens;             /* (host) T >= 0 */

@@ -119,8 +119,27 @@ struct TcTok {
     int32_t gathered_len;
 };
 
-__device__ __forceinline__ TcTok tc_token(const RowSource &R, int t) {
+// The layout half of token t's record (read before the kernel waits for the
+// preceding grid: no kernel of this library writes a layout while letting
+// its dependents start early).
+__device__ __forceinline__ TcTok tc_token_layout(const RowSource &R, int t) {
     TcTok k{};
+    if (R.fused == kRowsGathered) return k;
+    const TokenView v = token_view(R.L, R.ratio, t);
+    k.bad = v.bad;
+    if (v.bad & CSA_DEV_BAD_LAYOUT) return k;
+    k.first = window_first(v.pos, R.window);
+    k.nswa = R.no_window ? 0 : static_cast<int32_t>(v.pos - k.first + 1);
+    k.off = v.off;
+    k.n_vis = v.n_vis;
+    k.b = v.b;
+    k.first_res = R.L.swa_first_pos[v.b];
+    return k;
+}
+
+// The rest, after the wait: the selection count (or the gathered length)
+// the preceding kernels produced, and the slots that follow from it.
+__device__ __forceinline__ void tc_token_finish(const RowSource &R, int t, TcTok &k) {
     if (R.fused == kRowsGathered) {
         int32_t len = R.kv_len[t];
         if (len < 0 || len > R.rows_per_token) {
@@ -130,18 +149,15 @@ __device__ __forceinline__ TcTok tc_token(const RowSource &R, int t) {
         k.gathered_len = len;
         k.nsel = len;
         k.wslot = len;
-        return k;
+        return;
     }
+    if (k.bad & CSA_DEV_BAD_LAYOUT) return;
     // (the window's partial has no selection to read)
-    const int32_t ns_sel = (R.fused == kRowsSelected && !R.no_selected) ? R.n_sel[t] : 0;
-    const TokenView v = token_view(R.L, R.ratio, t);
-    k.bad = v.bad;
-    if (v.bad & CSA_DEV_BAD_LAYOUT) return k;
     int32_t ns;
     if (R.fused == kRowsAllVisible) {
-        ns = static_cast<int32_t>(v.n_vis);
+        ns = static_cast<int32_t>(k.n_vis);
     } else {
-        ns = ns_sel;
+        ns = (R.fused == kRowsSelected && !R.no_selected) ? R.n_sel[t] : 0;
         if (ns < 0 || ns > R.top_k) {
             k.bad |= CSA_DEV_BAD_LENGTH;
             ns = ns < 0 ? 0 : R.top_k;
@@ -150,13 +166,6 @@ __device__ __forceinline__ TcTok tc_token(const RowSource &R, int t) {
     if (R.no_selected) ns = 0;
     k.nsel = ns;
     k.wslot = (ns + 3) & ~3;
-    k.first = window_first(v.pos, R.window);
-    k.nswa = R.no_window ? 0 : static_cast<int32_t>(v.pos - k.first + 1);
-    k.off = v.off;
-    k.n_vis = v.n_vis;
-    k.b = v.b;
-    k.first_res = R.L.swa_first_pos[v.b];
-    return k;
 }
 
 __device__ __forceinline__ void tmem_ld16_raw(uint32_t taddr, uint32_t (&r)[16]) {
@@ -244,6 +253,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int bx = 0; bx < 8; ++bx)
             tma_load_2d(sQ + bx * (kHG * 128), &tm_q, bx * 64, y, &S.q_full, policy_evict_normal());
     };
+    // the token's row slots (one reader, shared): the layout half now
+    __shared__ TcTok tok_s;
+    if (tid == 0) tok_s = tc_token_layout(A.R, t);
     if (A.early_q && tid == 0) load_q();
     pdl_wait();
     pdl_launch_dependents();
@@ -259,10 +271,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int j = split * A.rows_split + kLdRows * li + lane;
         if (lane < kLdRows && j < A.R.top_k) pre_sidx = A.R.idx[static_cast<int64_t>(t) * A.R.top_k + j];
     }
-    // the token's row slots (one reader, shared)
-    __shared__ TcTok tok_s;
+    // ... and the selection half after the wait
     if (tid == 0) {
-        const TcTok kk = tc_token(A.R, t);
+        TcTok kk = tok_s;
+        tc_token_finish(A.R, t, kk);
         tok_s = kk;
         S.nslots = A.R.fused == kRowsGathered ? kk.gathered_len : kk.wslot + kk.nswa;
         if (split == 0 && hg == 0) raise_status(A.status, kk.bad);

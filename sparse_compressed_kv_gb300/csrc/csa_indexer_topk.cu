@@ -781,30 +781,10 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = S.tmem_holder;
 
-    // Inputs may come from the preceding grid in the stream.
-    pdl_wait();
-    // One token of one sequence: while the layout is read, warm L2 with this
-    // CTA's first keys as they fall when the token sees the whole cache (one
-    // bulk prefetch, from a warp that is idle until later).  A guess: a layout
-    // that says otherwise costs bandwidth, never data.
-    if (warp == 6 && lane == 0 && T == 1 && P.L.num_seqs == 1) {
-        const int64_t K32 = (P.L.max_comp_rows + kBoxRows - 1) / kBoxRows;
-        const int64_t Ge = K32 < G ? K32 : G;
-        if (c < Ge) {
-            const int64_t u0 = K32 * c / Ge, u1 = K32 * (c + 1) / Ge;
-            int64_t n = (u1 - u0) * kBoxRows;
-            n = n < kWarmKeys ? n : kWarmKeys;
-            const int64_t r0 = u0 * kBoxRows;
-            if (r0 + n > P.L.total_comp_rows) n = P.L.total_comp_rows - r0;
-            constexpr int64_t kRowB = kFp4 ? kFRow : 256;
-            if (n > 0)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(P.k_idx + r0 * kRowB),
-                             "r"(static_cast<uint32_t>(n * kRowB))
-                             : "memory");
-        }
-    }
-
-    // ---- every token's visible blocks and units (the same in every CTA)
+    // ---- every token's visible blocks and units (the same in every CTA).
+    // The layout is read before the wait for the preceding grid: no kernel
+    // of this library writes a layout while letting its dependents start
+    // early, and any other kernel has finished before this one starts.
     for (int t = tid; t < T; t += kCta) {
         const TokenView v = token_view(P.L, P.ratio, t);
         if (v.bad && c == 0) raise_status(P.status, v.bad);
@@ -821,6 +801,23 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreads, 1)
     const int Ge = static_cast<int>(K32 < G ? K32 : G);   // CTAs with work: one unit at least
     const int64_t ua = c < Ge ? K32 * c / Ge : K32;
     const int64_t ub = c < Ge ? K32 * (c + 1) / Ge : K32;
+    // The queries, weights and keys may come from the preceding grid.
+    pdl_wait();
+    // Warm L2 with the first keys of this CTA's range (one bulk prefetch, from
+    // a warp that is idle until later).
+    if (warp == 6 && lane == 0 && ua < ub) {
+        const int t0 = token_of(S.U, T, ua);
+        int64_t u1 = S.U[t0 + 1] < ub ? S.U[t0 + 1] : ub;
+        int64_t n = (u1 - ua) * kBoxRows;
+        n = n < kWarmKeys ? n : kWarmKeys;
+        const int64_t r0 = S.off[t0] + (ua - S.U[t0]) * kBoxRows;
+        if (r0 + n > P.L.total_comp_rows) n = P.L.total_comp_rows - r0;
+        constexpr int64_t kRowB = kFp4 ? kFRow : 256;
+        if (n > 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(P.k_idx + r0 * kRowB),
+                         "r"(static_cast<uint32_t>(n * kRowB))
+                         : "memory");
+    }
     // The next kernel may start its prologue; it waits for this grid to finish.
     pdl_launch_dependents();
 

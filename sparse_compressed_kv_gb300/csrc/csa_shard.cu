@@ -33,8 +33,9 @@ namespace {
 // token_view on the rewritten layout yields n' visible blocks at rows 0..n'-1.
 __global__ void shard_layout_kernel(const csa_layout_t L, int32_t ratio, int64_t lo, int64_t hi,
                                     int64_t *tok_pos_out, int64_t *comp_off_out, int32_t *status) {
+    // (no early start for the next kernel: the decode indexer reads the layout
+    // this kernel writes before it waits for the preceding grid)
     pdl_wait();
-    pdl_launch_dependents();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t == 0) {
         comp_off_out[0] = 0;
