@@ -314,3 +314,24 @@ def test_many_short_sequences(cuda_device, B):
     wl = W.make(f"many{B}", seed=B, seq_lens=seq_lens, tokens=[1] * B, n_comp=n_comp, top_k=16,
                 n_heads=16)
     full_chain(H.Run(wl, cuda_device), check_recall=False)
+
+
+def test_layout_rewritten_by_a_kernel_right_before(cuda_device):
+    # the layout is read as a kernel starts; a torch kernel that rewrites it
+    # just before the call (same stream, no synchronisation, no programmatic
+    # launch) has finished by then: each call must see the shrunken cache
+    wl = W.make("devlayout", seed=44, seq_lens=[4 * 3000], n_comp=[3000], top_k=256, n_heads=16)
+    run = H.Run(wl, cuda_device)
+    for k in range(1, 5):
+        run.d.comp_off[1:].sub_(37)          # a device kernel on the current stream
+        out, fidx = run.decode()
+        wl.comp_off[1:] -= 37                # the oracle's view of the same layout
+        sc = run.scores()
+        idx, n_sel = run.topk(sc)
+        H.check_topk_exact(wl, sc, idx, n_sel)
+        torch.cuda.synchronize()
+        assert int(n_sel[0]) == 256 and torch.equal(fidx, idx)
+        assert int(idx[0].max()) < 3000 - 37 * k
+        kv_buf, kv_len = H.gpu_rows(run, idx, n_sel)
+        H.check_attention(wl, kv_buf, kv_len, out)
+    assert run.dev_status() == 0
