@@ -39,6 +39,11 @@ WsPlan make_plan(int64_t T, int64_t max_comp_rows, const csa_params_t &p, int64_
     const int64_t per = (chunks + splits - 1) / splits;
     w.rows_split = static_cast<int32_t>(per * kTcChunk);
     w.splits = static_cast<int32_t>((slots + w.rows_split - 1) / w.rows_split);
+    // Still few CTAs (one long-context token): 2 or 4 CTAs per split, each
+    // computing the split's weights in full and accumulating and writing
+    // only its share of the 512 output columns.
+    const int64_t ctas = static_cast<int64_t>(w.splits) * (T > 0 ? T : 1) * groups;
+    w.dparts = ctas * 4 <= kAttnCtas ? 4 : (ctas * 2 <= kAttnCtas ? 2 : 1);
     const size_t A = 256;
     const size_t Tz = static_cast<size_t>(T > 0 ? T : 0);
     w.state_bytes = Tz * kStateWords * 4;

@@ -63,7 +63,7 @@ constexpr int kRowsBytes = 8 * kRowBox;        // 64 KiB per stage
 constexpr int kPBytes = kHG * kChunk * 2;      // 8 KiB: one bf16 term of P
 constexpr int kTmemCols = 512;
 constexpr int kSCol = 0;                       // S buffers: columns 0 .. 127
-constexpr int kOCol = 128;                     // O^T: 4 tiles x 64 heads
+constexpr int kOCol = 128;                     // O^T: up to 4 tiles x 64 heads
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleAbove = 8.f;           // log2 units
 
@@ -208,8 +208,15 @@ __device__ __forceinline__ constexpr uint32_t idesc_bf16() {
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// kDT: 128-column tiles of the output this CTA owns (4: all 512 columns;
+// 2 or 1 when 2 or 4 CTAs share a row split, each computing the split's
+// logits and weights in full and accumulating only its own columns).
+template <int kDT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const TcParams A) {
+    static_assert(kDT == 1 || kDT == 2 || kDT == 4, "1, 2 or 4 column tiles");
+    constexpr int kParts = 4 / kDT;
+    constexpr uint32_t kCols = kDT == 4 ? kTmemCols : kTmemCols / 2;   // S + O^T columns, a power of 2
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem<1024>(smem_raw);
     uint8_t *sQ = smem;
@@ -217,7 +224,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *sP = sRows + 2 * kRowsBytes;                  // [2 buffers][hi, lo][64 heads][128 B]
     TcSmem &S = *reinterpret_cast<TcSmem *>(sP + 4 * kPBytes);
 
-    const int split = blockIdx.x, hg = blockIdx.y, t = blockIdx.z;
+    const int split = blockIdx.x, t = blockIdx.z;
+    const int hg = static_cast<int>(blockIdx.y) / kParts;
+    const int dt0 = (static_cast<int>(blockIdx.y) % kParts) * kDT;   // first owned column tile
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h0 = hg * kHG;
     const int H = A.H;
@@ -237,7 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_q);
     }
     if (warp == 1) {
-        tmem_alloc(&S.tmem_holder, kTmemCols);
+        tmem_alloc(&S.tmem_holder, kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -277,7 +286,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_token_finish(A.R, t, kk);
         tok_s = kk;
         S.nslots = A.R.fused == kRowsGathered ? kk.gathered_len : kk.wslot + kk.nswa;
-        if (split == 0 && hg == 0) raise_status(A.status, kk.bad);
+        if (split == 0 && blockIdx.y == 0) raise_status(A.status, kk.bad);
     }
     __syncthreads();
     const int nslots = S.nslots;
@@ -309,21 +318,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 umma_commit(&S.sfull[st]);
             };
             // O^T[d][h] += sum_j rows[j][d] P[h][j] of chunk i (P written),
-            // per 128-column tile of d
+            // per owned 128-column tile of d
             auto pv = [&](int i) {
                 const int st = i & 1;
                 const uint32_t rows = r_base + st * kRowsBytes;
                 const uint32_t pb = p_base + st * 2 * kPBytes;
 #pragma unroll
-                for (int dt = 0; dt < 4; ++dt)
+                for (int dd = 0; dd < kDT; ++dd)
 #pragma unroll
                     for (int ks = 0; ks < kChunk / 16; ++ks) {
                         const uint64_t adesc =
-                            sw128_desc(rows + (2 * dt) * kRowBox + ks * 16 * 128, kRowBox, 1024);
+                            sw128_desc(rows + (2 * (dt0 + dd)) * kRowBox + ks * 16 * 128, kRowBox, 1024);
                         const uint32_t acc0 = (i > 0 || ks > 0) ? 1u : 0u;
-                        umma_bf16(tmem + kOCol + dt * kHG, adesc, sw128_desc(pb + ks * 32, 16, 1024),
+                        umma_bf16(tmem + kOCol + dd * kHG, adesc, sw128_desc(pb + ks * 32, 16, 1024),
                                   id_pv, acc0);
-                        umma_bf16(tmem + kOCol + dt * kHG, adesc,
+                        umma_bf16(tmem + kOCol + dd * kHG, adesc,
                                   sw128_desc(pb + kPBytes + ks * 32, 16, 1024), id_pv, 1u);
                     }
                 umma_commit(&S.empty[st]);
@@ -503,11 +512,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 named_bar_sync(kBarSm, kSmThreads);
                 tc_fence_after();
 #pragma unroll 1
-                for (int dt = 0; dt < 4; ++dt)
+                for (int dd = 0; dd < kDT; ++dd)
 #pragma unroll 1
                     for (int hb = 0; hb < 4; ++hb) {
                         uint32_t r[16];
-                        const uint32_t ta = tmem + lane_off + kOCol + dt * kHG + hb * 16;
+                        const uint32_t ta = tmem + lane_off + kOCol + dd * kHG + hb * 16;
                         tmem_ld16_raw(ta, r);
                         tmem_wait_ld();
 #pragma unroll
@@ -575,34 +584,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int hmax = min(kHG, H - h0);
         // one output column per lane: every warp store is 128 contiguous bytes
         if (nch == 0) {
-            for (int e = st_t; e < hmax * kHD; e += kSmThreads) dst[obase + e] = 0.f;
+            for (int e = st_t; e < hmax * 128 * kDT; e += kSmThreads)
+                dst[obase + (e / (128 * kDT)) * kHD + dt0 * 128 + e % (128 * kDT)] = 0.f;
         } else {
 #pragma unroll 1
-            for (int dt = 0; dt < 4; ++dt) {
-                const int d = dt * 128 + q * 32 + lane;
+            for (int dd = 0; dd < kDT; ++dd) {
+                const int d = (dt0 + dd) * 128 + q * 32 + lane;
                 uint32_t r[4][16];
 #pragma unroll
-                for (int hb = 0; hb < 4; ++hb) tmem_ld16_raw(tmem + lane_off + kOCol + dt * kHG + hb * 16, r[hb]);
+                for (int hb = 0; hb < 4; ++hb) tmem_ld16_raw(tmem + lane_off + kOCol + dd * kHG + hb * 16, r[hb]);
                 tmem_wait_ld();
-                float *dd = dst + obase + d;
+                float *od = dst + obase + d;
                 if (part && hmax == kHG) {
                     // a raw partial of a full head group: no scale, no head bound
 #pragma unroll
                     for (int hb = 0; hb < 4; ++hb)
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) dd[(hb * 16 + c) * kHD] = __uint_as_float(r[hb][c]);
+                        for (int c = 0; c < 16; ++c) od[(hb * 16 + c) * kHD] = __uint_as_float(r[hb][c]);
                 } else {
 #pragma unroll
                     for (int hb = 0; hb < 4; ++hb)
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const int h = hb * 16 + c;
-                            if (h < hmax) dd[h * kHD] = __uint_as_float(r[hb][c]) * S.fin[h];
+                            if (h < hmax) od[h * kHD] = __uint_as_float(r[hb][c]) * S.fin[h];
                         }
                 }
             }
         }
-        if (part && !upper && hv) {
+        if (part && !upper && hv && dt0 == 0) {
             const int64_t mb = ((static_cast<int64_t>(t) * A.splits + split) * H + h0 + hl) * 2;
             A.part_ml[mb + 0] = nch > 0 ? m_ref : -INFINITY;
             A.part_ml[mb + 1] = nch > 0 ? l : 0.f;
@@ -612,7 +622,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, kCols);
     }
 }
 
@@ -752,10 +762,14 @@ cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t 
         A.part_ml = raw_ml;
     }
     const size_t smem = attention_tc_smem_bytes();
-    cudaError_t e = set_kernel_smem(attention_tc_kernel, smem);
+    // dparts CTAs per (row split, head group), each owning 4 / dparts of the
+    // output's 128-column tiles
+    void (*kern)(const CUtensorMap, const TcParams) =
+        plan.dparts == 4 ? attention_tc_kernel<1> : plan.dparts == 2 ? attention_tc_kernel<2> : attention_tc_kernel<4>;
+    cudaError_t e = set_kernel_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(plan.splits, (H + kHG - 1) / kHG, T);
-    e = launch_pdl(attention_tc_kernel, grid, dim3(kTcThreads), smem, lc.stream, tq, A);
+    dim3 grid(plan.splits, ((H + kHG - 1) / kHG) * plan.dparts, T);
+    e = launch_pdl(kern, grid, dim3(kTcThreads), smem, lc.stream, tq, A);
     if (e != cudaSuccess || plan.splits == 1) return e;
     // splits <= kMaxSplits (the plan's cap): nsub <= 8, blockDim <= 1024
     if (plan.splits > kMaxSplits) return cudaErrorInvalidValue;

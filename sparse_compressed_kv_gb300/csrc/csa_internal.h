@@ -40,6 +40,7 @@ struct WsPlan {
     int32_t topk_per_tok = 1;  // top-k filter CTAs per token (1: one CTA owns the row)
     int32_t splits = 1;      // attention splits per token
     int32_t rows_split = 0;  // rows per attention split (multiple of kTcChunk)
+    int32_t dparts = 1;      // attention CTAs per split and head group (1, 2 or 4), one column range each
     // Layout: [per-token state | ... free ... | data].  The state slots sit at
     // the front at offsets that depend only on the token index; the data
     // regions are packed against the end of the caller's workspace, so no
