@@ -260,6 +260,21 @@ def _flat():
     return wl
 
 
+def _one_bin(name, seed, n, k):
+    # every score in [1.27, 1.47], inside one first-level radix bin (a quarter
+    # octave): the threshold bin holds all n candidates, so the cut is
+    # settled entirely by the digits below the first
+    wl = W.make(name, seed=seed, seq_lens=[4 * n], n_comp=[n], top_k=k, n_heads=16)
+    g = torch.Generator().manual_seed(seed)
+    v = torch.randn(wl.ihd, generator=g)
+    v = v / v.norm()
+    wl.q_idx[0] = v.to(torch.bfloat16)[None, :].expand(wl.n_ih, -1)
+    wl.w_idx.fill_(1.0 / wl.n_ih)
+    a = 1.27 + 0.2 * torch.rand(n, generator=g)
+    wl.k_idx[:n] = (a[:, None] * v[None, :]).to(torch.bfloat16)
+    return wl
+
+
 def _signs():
     wl = W.make("signs2", seed=33, seq_lens=[4 * 3000], n_comp=[3000], top_k=300, n_heads=16)
     wl.w_idx.copy_(-wl.w_idx.abs())
@@ -277,6 +292,8 @@ INDEXER_TOPK_CASES = {
     "chunk": lambda: W.make("chunk2", seed=36, seq_lens=[4 * 700], tokens=[37], top_k=128,
                             n_heads=16, swa_cap=256),
     "ties": _ties, "flat": _flat, "signs": _signs, "monotone": _monotone,
+    "one_bin_2k": lambda: _one_bin("onebin1", 37, 2040, 1000),
+    "one_bin_10k": lambda: _one_bin("onebin2", 38, 10000, 1024),
 }
 
 
@@ -296,6 +313,9 @@ def test_indexer_topk_equals_topk_on_the_scores(cuda_device, name):
         torch.cuda.synchronize()
         assert torch.equal(n_sel, ref_n)
         assert torch.equal(idx, ref_idx)
+    if name.startswith("one_bin"):
+        s = sc.cpu()[0, :wl.total_comp_rows]
+        assert float(s.min()) > 1.25 and float(s.max()) < 1.5
     if name == "monotone":
         # the selection is the tail of the cache (rounding may swap neighbours)
         assert idx.cpu().numpy()[0].min() >= 1800
