@@ -627,29 +627,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // out[t,h,:] = sum_s 2^(m_s - M) O_s / (sum_s 2^(m_s - M) l_s [+ 2^(sink log2e - M)]),
-// splits without rows (m = -inf) skipped.  CTA = (head, token); thread
-// (sub, c4) holds columns 4 c4 .. 4 c4 + 3 of splits sub, sub + nsub, ...,
-// loaded kCombPer at a time (all of them in flight), and the nsub partial
-// sums meet in shared memory in a fixed order.
+// splits without rows (m = -inf) skipped.  CTA = (head, token) of 128 nsub
+// threads and one more warp: thread (sub, c4) holds columns 4 c4 .. 4 c4 + 3
+// of splits sub, sub + nsub, ..., loaded kCombPer at a time (all of them in
+// flight), the last warp reads every split's (m, l) meanwhile, and the nsub
+// partial sums meet in shared memory in a fixed order.
 constexpr int kCombPer = 8;
 constexpr int kMaxSplits = 256;
-constexpr int kMlPer = kMaxSplits / 32;    // (m, l) pairs per lane of the first warp
+constexpr int kMlPer = kMaxSplits / 32;    // (m, l) pairs per lane of the last warp
+constexpr int kCombMaxSub = 7;
+constexpr int kCombMaxThreads = 128 * kCombMaxSub + 32;
 
-__global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
+__global__ void __launch_bounds__(kCombMaxThreads) combine_tc_kernel(const TcParams A) {
     pdl_wait();
     pdl_launch_dependents();
     const int h = blockIdx.x, t = blockIdx.y;
     if (!CSA_CHECK(A.splits <= kMaxSplits, A.status)) return;
-    const int nsub = static_cast<int>(blockDim.x >> 7);
+    const int nsub = static_cast<int>((blockDim.x - 32) >> 7);
+    const bool ml_warp = static_cast<int>(threadIdx.x) >= 128 * nsub;
     const int c4 = threadIdx.x & 127, sub = threadIdx.x >> 7;
     __shared__ float wgt[kMaxSplits];
     __shared__ float inv_z;
-    __shared__ float4 red[7][128];
+    __shared__ float4 red[kCombMaxSub - 1][128];
     const int ns = A.splits;
     const float *mlb = A.part_ml + t * A.ml_t + h * 2;
     const int64_t mstride = A.ml_s;
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
+    // the first kCombPer of a thread's partial columns are in flight while
+    // the last warp reads (m, l) (every split writes its partial, zeros when
+    // it has no rows, so the loads need not wait for the weights)
+    const float *pb = A.part_o + t * A.po_t + h * kHD + 4 * c4;
+    const int64_t pstride = A.po_s;
+    float4 v[kCombPer];
+    if (!ml_warp) {
+#pragma unroll
+        for (int k = 0; k < kCombPer; ++k) {
+            const int sp = sub + k * nsub;
+            if (sp < ns) v[k] = __ldcg(reinterpret_cast<const float4 *>(pb + sp * pstride));
+        }
+    } else {
+        const int lane = threadIdx.x & 31;
         float m[kMlPer], lv[kMlPer];
 #pragma unroll
         for (int k = 0; k < kMlPer; ++k) {
@@ -691,15 +707,14 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
         }
     }
     __syncthreads();
-    const float *pb = A.part_o + t * A.po_t + h * kHD + 4 * c4;
-    const int64_t pstride = A.po_s;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = sub; base < ns; base += kCombPer * nsub) {
-        float4 v[kCombPer];
+    for (int base = sub; !ml_warp && base < ns; base += kCombPer * nsub) {
+        if (base != sub) {
 #pragma unroll
-        for (int k = 0; k < kCombPer; ++k) {
-            const int sp = base + k * nsub;
-            if (sp < ns && wgt[sp] != 0.f) v[k] = __ldcg(reinterpret_cast<const float4 *>(pb + sp * pstride));
+            for (int k = 0; k < kCombPer; ++k) {
+                const int sp = base + k * nsub;
+                if (sp < ns && wgt[sp] != 0.f) v[k] = __ldcg(reinterpret_cast<const float4 *>(pb + sp * pstride));
+            }
         }
 #pragma unroll
         for (int k = 0; k < kCombPer; ++k) {
@@ -713,7 +728,7 @@ __global__ void __launch_bounds__(1024) combine_tc_kernel(const TcParams A) {
             }
         }
     }
-    if (sub > 0) red[sub - 1][c4] = acc;
+    if (sub > 0 && !ml_warp) red[sub - 1][c4] = acc;
     __syncthreads();
     if (sub == 0) {
         for (int j = 0; j + 1 < nsub; ++j) {
@@ -771,7 +786,6 @@ cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t 
     dim3 grid(plan.splits, ((H + kHG - 1) / kHG) * plan.dparts, T);
     e = launch_pdl(kern, grid, dim3(kTcThreads), smem, lc.stream, tq, A);
     if (e != cudaSuccess || plan.splits == 1) return e;
-    // splits <= kMaxSplits (the plan's cap): nsub <= 8, blockDim <= 1024
     if (plan.splits > kMaxSplits) return cudaErrorInvalidValue;
     A.po_t = static_cast<int64_t>(plan.splits) * H * kHD;
     A.po_s = static_cast<int64_t>(H) * kHD;
@@ -779,10 +793,10 @@ cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t 
     A.ml_s = static_cast<int64_t>(H) * 2;
     A.raw_ml = raw_ml;
     int nsub = (plan.splits + kCombPer - 1) / kCombPer;
-    nsub = nsub < 8 ? nsub : 8;
+    nsub = nsub < kCombMaxSub ? nsub : kCombMaxSub;
     e = set_kernel_smem(combine_tc_kernel, 0);
     if (e != cudaSuccess) return e;
-    return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub), 0, lc.stream, A);
+    return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub + 32), 0, lc.stream, A);
 }
 
 cudaError_t launch_partials_combine(const Launch &lc, int32_t P, int32_t T, int32_t H,
@@ -803,10 +817,10 @@ cudaError_t launch_partials_combine(const Launch &lc, int32_t P, int32_t T, int3
     A.ml_t = static_cast<int64_t>(H) * 2;
     A.ml_s = static_cast<int64_t>(T) * H * 2;
     int nsub = (P + kCombPer - 1) / kCombPer;
-    nsub = nsub < 8 ? nsub : 8;
+    nsub = nsub < kCombMaxSub ? nsub : kCombMaxSub;
     cudaError_t e = set_kernel_smem(combine_tc_kernel, 0);
     if (e != cudaSuccess) return e;
-    return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub), 0, lc.stream, A);
+    return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub + 32), 0, lc.stream, A);
 }
 
 }  // namespace csa
