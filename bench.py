@@ -261,7 +261,7 @@ def check_status(status, where):
         raise RuntimeError(f"device status {st:#x} in the {where} region")
 
 
-def e2e_leg(layers, step, stream, steps, warmup, world, passes: int = 4):
+def e2e_leg(layers, step, stream, steps, warmup, world, passes: int = 8):
     """The step through the public API with host buffers: every step copies
     its activations from pinned host memory, runs csa_decode and copies the
     output back to pinned host memory, all inside the timed region.  As a
