@@ -66,6 +66,7 @@ constexpr int kABytes = 2 * kHalfBytes;        // 32 KiB per stage
 constexpr int kBoxBytes = kBoxRows * 128;      // 4 KiB: one 32-row box of one half
 constexpr int kBBytes = 2 * kN * 128;          // 16 KiB: one token's queries
 constexpr int kStageEntries = kStages * kABytes / 8;  // resolver staging in the ring
+static_assert(kStageEntries < 65536, "the resolve packs two entry counts in one word");
 // FP4 keys (80-byte MXFP4 rows): a ring of raw code tiles in shared memory.
 // Four warps, one per TMEM lane quarter (8, 9, 6, 7), expand each tile into
 // f16 keys in tensor memory, where the MMA reads its A operand; no f16 tile
@@ -364,6 +365,22 @@ __device__ __forceinline__ void finalize_segment(const DecParams &P, DecSmem &S,
 // key of every finite score, so it is never selected.
 constexpr uint64_t kNoEntry = 0xffffffffull;
 
+// f(e) for each staged entry of a thread's run [r0, r1), the entries loaded
+// eight at a time ahead of the work on them: shared-memory atomics in that
+// work would otherwise hold each following load behind them.
+template <typename F>
+__device__ __forceinline__ void for_run(const uint64_t *stage, int r0, int r1, F &&f) {
+#pragma unroll 1
+    for (int b = r0; b < r1; b += 8) {
+        uint64_t e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) e[k] = b + k < r1 ? stage[b + k] : 0ull;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (b + k < r1) f(e[k]);
+    }
+}
+
 // The exact top-k of token t, from the candidates of its segments or, when
 // they do not prove the result, from its whole score row.  Whole CTA.
 __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, uint64_t *stage,
@@ -439,11 +456,10 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
         uint32_t need = kk - S.fgt;
         const int R = odd_run(static_cast<int>(M), kThreads);
         const int r0 = min(static_cast<int>(M), tid * R), r1 = min(static_cast<int>(M), r0 + R);
-#pragma unroll 4
-        for (int i = r0; i < r1; ++i) {
-            const uint32_t key = static_cast<uint32_t>(stage[i] >> 32);
+        for_run(stage, r0, r1, [&](uint64_t e) {
+            const uint32_t key = static_cast<uint32_t>(e >> 32);
             if ((key >> kD1Shift) == d1) atomicAdd(&h2[(key >> kD2Shift) & (kD2Bins - 1)], 1u);
-        }
+        });
         main_sync();
         {
             uint32_t v[8];
@@ -452,11 +468,10 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
         }
         const uint32_t pre = (d1 << kD2Bits) | static_cast<uint32_t>(S.fd);
         need -= S.fgt;
-#pragma unroll 4
-        for (int i = r0; i < r1; ++i) {
-            const uint32_t key = static_cast<uint32_t>(stage[i] >> 32);
+        for_run(stage, r0, r1, [&](uint64_t e) {
+            const uint32_t key = static_cast<uint32_t>(e >> 32);
             if ((key >> kD2Shift) == pre) atomicAdd(&h3[key & (kD3Bins - 1)], 1u);
-        }
+        });
         main_sync();
         {
             uint32_t v[4];
@@ -466,26 +481,21 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
         const uint32_t tau = (pre << kD2Shift) | static_cast<uint32_t>(S.fd);
         need -= S.fgt;
         const bool all_ties = need == h3[S.fd];
-        // ties at tau before this thread's run
-        uint32_t tb = 0;
-        if (!all_ties) {
-            uint32_t ties = 0;
+        // one pass and one block scan: the entries above tau and the ties at
+        // tau before this thread's run (packed, each count below 2^16); the
+        // ties are taken in block order, the first `need` of them
+        uint32_t ties = 0, gt = 0;
 #pragma unroll 4
-            for (int i = r0; i < r1; ++i) ties += static_cast<uint32_t>(stage[i] >> 32) == tau ? 1u : 0u;
-            tb = group_scan<kWarps>(ties, S.bscan, warp, 0, nullptr);
+        for (int i = r0; i < r1; ++i) {
+            const uint32_t key = static_cast<uint32_t>(stage[i] >> 32);
+            ties += key == tau ? 1u : 0u;
+            gt += key > tau ? 1u : 0u;
         }
-        uint32_t sel = 0;
-        {
-            uint32_t r = tb;
-#pragma unroll 4
-            for (int i = r0; i < r1; ++i) {
-                const uint32_t key = static_cast<uint32_t>(stage[i] >> 32);
-                const bool tie = key == tau;
-                sel += (key > tau || (tie && (all_ties || r < need))) ? 1u : 0u;
-                r += tie ? 1u : 0u;
-            }
-        }
-        uint32_t pos = group_scan<kWarps>(sel, S.bt, warp, 0, &total);
+        uint32_t both = 0;
+        const uint32_t before = group_scan<kWarps>(gt | (ties << 16), S.bt, warp, 0, &both);
+        const uint32_t tb = before >> 16;
+        uint32_t pos = (before & 0xffffu) + (all_ties ? tb : min(tb, need));
+        total = (both & 0xffffu) + (all_ties ? (both >> 16) : min(both >> 16, need));
         uint32_t r = tb;
 #pragma unroll 4
         for (int i = r0; i < r1; ++i) {
@@ -493,8 +503,7 @@ __device__ __forceinline__ void resolve_token(const DecParams &P, DecSmem &S, ui
             const uint32_t key = static_cast<uint32_t>(e >> 32);
             const bool tie = key == tau;
             if (key > tau || (tie && (all_ties || r < need))) {
-                const int64_t blk = static_cast<int64_t>(e & 0xffffffffu);
-                if (pos < kk) out[pos] = static_cast<int32_t>(blk);
+                if (pos < kk) out[pos] = static_cast<int32_t>(e & 0xffffffffu);
                 ++pos;
             }
             r += tie ? 1u : 0u;
