@@ -300,20 +300,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_wait(&S.q_full, 0, A.status);
             constexpr uint32_t id_qk = idesc_bf16<kHG, kChunk, false>();
             constexpr uint32_t id_pv = idesc_bf16<128, kHG, true>();
-            const uint32_t q_base = smem_addr(sQ);
-            const uint32_t r_base = smem_addr(sRows);
-            const uint32_t p_base = smem_addr(sP);
+            // Descriptors are built once and stepped by adding an operand's
+            // byte offset / 16 to the start-address field (every shared
+            // address is below 256 KiB, so the 14-bit field never carries):
+            // building one per instruction made the issuing thread, not the
+            // tensor pipe, set the pace of these small MMAs.
+            const uint64_t q_desc = sw128_desc(smem_addr(sQ), 16, 1024);
+            const uint64_t r_desc = sw128_desc(smem_addr(sRows), 16, 1024);
+            const uint64_t a_desc = sw128_desc(smem_addr(sRows) + (2 * dt0) * kRowBox, kRowBox, 1024);
+            const uint64_t p_desc = sw128_desc(smem_addr(sP), 16, 1024);
+            auto off = [](uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); };
             // S = Q . rows^T of chunk i, into S buffer i % 2 (rows landed,
             // the S buffer read by the softmax)
             auto qk = [&](int i) {
                 const int st = i & 1;
-                const uint32_t rows = r_base + st * kRowsBytes;
+                const uint64_t rd = r_desc + off(st * kRowsBytes);
+                const uint32_t d = tmem + kSCol + st * kChunk;
 #pragma unroll
                 for (int kk = 0; kk < 32; ++kk) {
                     const uint32_t bx = kk >> 2, ko = (kk & 3) * 32;
-                    umma_bf16(tmem + kSCol + st * kChunk,
-                              sw128_desc(q_base + bx * (kHG * 128) + ko, 16, 1024),
-                              sw128_desc(rows + bx * kRowBox + ko, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
+                    umma_bf16(d, q_desc + off(bx * (kHG * 128) + ko), rd + off(bx * kRowBox + ko), id_qk,
+                              kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&S.sfull[st]);
             };
@@ -321,19 +328,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // per owned 128-column tile of d
             auto pv = [&](int i) {
                 const int st = i & 1;
-                const uint32_t rows = r_base + st * kRowsBytes;
-                const uint32_t pb = p_base + st * 2 * kPBytes;
+                const uint64_t ad = a_desc + off(st * kRowsBytes);
+                const uint64_t pd = p_desc + off(st * 2 * kPBytes);
 #pragma unroll
                 for (int dd = 0; dd < kDT; ++dd)
 #pragma unroll
                     for (int ks = 0; ks < kChunk / 16; ++ks) {
-                        const uint64_t adesc =
-                            sw128_desc(rows + (2 * (dt0 + dd)) * kRowBox + ks * 16 * 128, kRowBox, 1024);
+                        const uint64_t adesc = ad + off((2 * dd) * kRowBox + ks * 16 * 128);
                         const uint32_t acc0 = (i > 0 || ks > 0) ? 1u : 0u;
-                        umma_bf16(tmem + kOCol + dd * kHG, adesc, sw128_desc(pb + ks * 32, 16, 1024),
-                                  id_pv, acc0);
-                        umma_bf16(tmem + kOCol + dd * kHG, adesc,
-                                  sw128_desc(pb + kPBytes + ks * 32, 16, 1024), id_pv, 1u);
+                        umma_bf16(tmem + kOCol + dd * kHG, adesc, pd + off(ks * 32), id_pv, acc0);
+                        umma_bf16(tmem + kOCol + dd * kHG, adesc, pd + off(kPBytes + ks * 32), id_pv, 1u);
                     }
                 umma_commit(&S.empty[st]);
                 umma_commit(&S.pfree[st]);
