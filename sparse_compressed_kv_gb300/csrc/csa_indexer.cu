@@ -291,8 +291,10 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp4>::kThreads, 1)
             int unit = find_unit(prefix, nu, u0), cur = -1;
             uint32_t gsw = 0;
             int it = 0;
-            const uint32_t a_base = smem_addr(sA);
-            const uint32_t b_base = smem_addr(sB);
+            // descriptors built once, stepped by byte offset / 16 (shared
+            // addresses stay below 256 KiB: the start-address field never carries)
+            const uint64_t a_desc = sw128_kmajor_desc(smem_addr(sA));
+            const uint64_t b_desc = sw128_kmajor_desc(smem_addr(sB));
             for (int u = u0; u < u1; ++u, ++it) {
                 while (u >= prefix[unit + 1]) ++unit;
                 if (unit != cur) {
@@ -309,13 +311,12 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp4>::kThreads, 1)
                 if (!mbar_wait(&a_full[stage], ph, P.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kN);
-                const uint32_t a_st = a_base + stage * C::kABytes;
+                const uint64_t a_st = a_desc + static_cast<uint64_t>((stage * C::kABytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kIHD / 16; ++kk) {
-                    const uint32_t a_addr = a_st + (kk >> 2) * C::kABox + (kk & 3) * 32;
-                    const uint32_t b_addr = b_base + (kk >> 2) * C::kBBox + (kk & 3) * 32;
-                    umma_bf16(d_tmem, sw128_kmajor_desc(a_addr), sw128_kmajor_desc(b_addr), idesc,
-                              kk > 0 ? 1u : 0u);
+                    const uint32_t a_off = (kk >> 2) * C::kABox + (kk & 3) * 32;
+                    const uint32_t b_off = (kk >> 2) * C::kBBox + (kk & 3) * 32;
+                    umma_bf16(d_tmem, a_st + (a_off >> 4), b_desc + (b_off >> 4), idesc, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&a_empty[stage]);
                 umma_commit(&acc_full[acc]);
