@@ -631,35 +631,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // out[t,h,:] = sum_s 2^(m_s - M) O_s / (sum_s 2^(m_s - M) l_s [+ 2^(sink log2e - M)]),
-// splits without rows (m = -inf) skipped.  CTA = (head, token) of 128 nsub
-// threads and one more warp: thread (sub, c4) holds columns 4 c4 .. 4 c4 + 3
-// of splits sub, sub + nsub, ..., loaded kCombPer at a time (all of them in
-// flight), the last warp reads every split's (m, l) meanwhile, and the nsub
-// partial sums meet in shared memory in a fixed order.
+// splits without rows (m = -inf) skipped.  CTA = (head, token, column part)
+// of cw nsub threads and one more warp, cw = 128 / parts: thread (sub, c4)
+// holds columns 4 c4 .. 4 c4 + 3 of the part for splits sub, sub + nsub,
+// ..., loaded kCombPer at a time (all of them in flight), the last warp reads
+// every split's (m, l) meanwhile, and the nsub partial sums meet in shared
+// memory in a fixed order.  Many splits: 4 parts of 128 columns (each CTA
+// reads a quarter of the partials); few: one part, fewer and larger CTAs.
 constexpr int kCombPer = 8;
 constexpr int kMaxSplits = 256;
 constexpr int kMlPer = kMaxSplits / 32;    // (m, l) pairs per lane of the last warp
-constexpr int kCombMaxSub = 7;
-constexpr int kCombMaxThreads = 128 * kCombMaxSub + 32;
+constexpr int kCombWideSub = 7;            // one part: at most 7 x 128 column threads
+constexpr int kCombMaxSub = 31;            // four parts: at most 31 x 32
+constexpr int kCombMaxThreads = 32 * kCombMaxSub + 32;
+constexpr int kCombRed = 960;              // partial sums of subs 1..: 30 x 32 or 6 x 128
+static_assert((kCombMaxSub - 1) * 32 <= kCombRed && (kCombWideSub - 1) * 128 <= kCombRed, "combine sums");
 
+template <int kCw>   // column threads per sub: 128 (one part) or 32 (four parts)
 __global__ void __launch_bounds__(kCombMaxThreads) combine_tc_kernel(const TcParams A) {
     pdl_wait();
     pdl_launch_dependents();
     const int h = blockIdx.x, t = blockIdx.y;
     if (!CSA_CHECK(A.splits <= kMaxSplits, A.status)) return;
-    const int nsub = static_cast<int>((blockDim.x - 32) >> 7);
-    const bool ml_warp = static_cast<int>(threadIdx.x) >= 128 * nsub;
-    const int c4 = threadIdx.x & 127, sub = threadIdx.x >> 7;
+    constexpr int cw = kCw;
+    const int nsub = (static_cast<int>(blockDim.x) - 32) / cw;
+    const bool ml_warp = static_cast<int>(threadIdx.x) >= cw * nsub;
+    const int c4 = static_cast<int>(threadIdx.x) % cw, sub = static_cast<int>(threadIdx.x) / cw;
+    const int col = static_cast<int>(blockIdx.z) * 4 * cw + 4 * c4;
     __shared__ float wgt[kMaxSplits];
     __shared__ float inv_z;
-    __shared__ float4 red[kCombMaxSub - 1][128];
+    __shared__ float4 red[kCombRed];
     const int ns = A.splits;
     const float *mlb = A.part_ml + t * A.ml_t + h * 2;
     const int64_t mstride = A.ml_s;
     // the first kCombPer of a thread's partial columns are in flight while
     // the last warp reads (m, l) (every split writes its partial, zeros when
     // it has no rows, so the loads need not wait for the weights)
-    const float *pb = A.part_o + t * A.po_t + h * kHD + 4 * c4;
+    const float *pb = A.part_o + t * A.po_t + h * kHD + col;
     const int64_t pstride = A.po_s;
     float4 v[kCombPer];
     if (!ml_warp) {
@@ -701,8 +709,10 @@ __global__ void __launch_bounds__(kCombMaxThreads) combine_tc_kernel(const TcPar
             const bool any = M != -INFINITY;
             if (A.raw_ml) {
                 // the merged partial: O scaled to M, l = sum_s 2^(m_s - M) l_s
-                A.raw_ml[(static_cast<int64_t>(t) * A.H + h) * 2 + 0] = M;
-                A.raw_ml[(static_cast<int64_t>(t) * A.H + h) * 2 + 1] = any ? z : 0.f;
+                if (blockIdx.z == 0) {
+                    A.raw_ml[(static_cast<int64_t>(t) * A.H + h) * 2 + 0] = M;
+                    A.raw_ml[(static_cast<int64_t>(t) * A.H + h) * 2 + 1] = any ? z : 0.f;
+                }
                 inv_z = 1.f;
             } else {
                 if (A.sinks && any) z += exp2f(sink - Mall);
@@ -732,20 +742,32 @@ __global__ void __launch_bounds__(kCombMaxThreads) combine_tc_kernel(const TcPar
             }
         }
     }
-    if (sub > 0 && !ml_warp) red[sub - 1][c4] = acc;
+    if (sub > 0 && !ml_warp) red[(sub - 1) * cw + c4] = acc;
     __syncthreads();
     if (sub == 0) {
         for (int j = 0; j + 1 < nsub; ++j) {
-            const float4 r = red[j][c4];
+            const float4 r = red[j * cw + c4];
             acc.x += r.x;
             acc.y += r.y;
             acc.z += r.z;
             acc.w += r.w;
         }
         const float iz = inv_z;
-        float *o = A.out + (static_cast<int64_t>(t) * A.H + h) * kHD + 4 * c4;
+        float *o = A.out + (static_cast<int64_t>(t) * A.H + h) * kHD + col;
         *reinterpret_cast<float4 *>(o) = make_float4(acc.x * iz, acc.y * iz, acc.z * iz, acc.w * iz);
     }
+}
+
+// The combine's launch shape for ns splits: one part while 7 subs of 128
+// column threads hold every split in one round of loads, else four parts.
+struct CombShape {
+    int parts, threads;
+    void (*kernel)(const TcParams);
+};
+CombShape comb_shape(int ns) {
+    const int nsub = (ns + kCombPer - 1) / kCombPer;
+    if (nsub <= kCombWideSub) return {1, 128 * nsub + 32, combine_tc_kernel<128>};
+    return {4, 32 * (nsub < kCombMaxSub ? nsub : kCombMaxSub) + 32, combine_tc_kernel<32>};
 }
 
 }  // namespace
@@ -796,11 +818,10 @@ cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t 
     A.ml_t = static_cast<int64_t>(plan.splits) * H * 2;
     A.ml_s = static_cast<int64_t>(H) * 2;
     A.raw_ml = raw_ml;
-    int nsub = (plan.splits + kCombPer - 1) / kCombPer;
-    nsub = nsub < kCombMaxSub ? nsub : kCombMaxSub;
-    e = set_kernel_smem(combine_tc_kernel, 0);
+    const CombShape cs = comb_shape(plan.splits);
+    e = set_kernel_smem(cs.kernel, 0);
     if (e != cudaSuccess) return e;
-    return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub + 32), 0, lc.stream, A);
+    return launch_pdl(cs.kernel, dim3(H, T, cs.parts), dim3(cs.threads), 0, lc.stream, A);
 }
 
 cudaError_t launch_partials_combine(const Launch &lc, int32_t P, int32_t T, int32_t H,
@@ -820,11 +841,10 @@ cudaError_t launch_partials_combine(const Launch &lc, int32_t P, int32_t T, int3
     A.po_s = static_cast<int64_t>(T) * H * kHD;
     A.ml_t = static_cast<int64_t>(H) * 2;
     A.ml_s = static_cast<int64_t>(T) * H * 2;
-    int nsub = (P + kCombPer - 1) / kCombPer;
-    nsub = nsub < kCombMaxSub ? nsub : kCombMaxSub;
-    cudaError_t e = set_kernel_smem(combine_tc_kernel, 0);
+    const CombShape cs = comb_shape(P);
+    cudaError_t e = set_kernel_smem(cs.kernel, 0);
     if (e != cudaSuccess) return e;
-    return launch_pdl(combine_tc_kernel, dim3(H, T), dim3(128 * nsub + 32), 0, lc.stream, A);
+    return launch_pdl(cs.kernel, dim3(H, T, cs.parts), dim3(cs.threads), 0, lc.stream, A);
 }
 
 }  // namespace csa
