@@ -267,19 +267,43 @@ def e2e_leg(layers, step, stream, steps, warmup, world, passes: int = 8):
     output back to pinned host memory, all inside the timed region.  As a
     serving loop overlaps them, one CUDA graph holds `passes` rounds of one
     step per rotating layer, with two device sets of each layer's inputs and
-    output (alternate rounds): the input copies run on their own stream as
-    soon as the decode two rounds back has read the set, each output copy on
+    output (alternate rounds): each step's input copy (its three inputs
+    packed in one pinned buffer) runs on its own stream as soon as the
+    decode two rounds back has read the set, each output copy on
     a third stream right behind its decode, and the decode stream waits once
     per round (for that round's inputs and for the output copies two rounds
     back), so consecutive decodes keep their programmatic launch overlap;
     value = steps / time over whole replays.  `step(L, s, ins, out)` runs one
     decode of layer L on inputs `ins` = (q_idx, w_idx, q) into `out`."""
     nl = len(layers)
-    hin = [(L.d.q_idx.cpu().pin_memory(), L.d.w_idx.cpu().pin_memory(),
-            L.d.q.cpu().pin_memory()) for L in layers]
+
+    def packed(like, device, pin):
+        # the step's three inputs back to back in one byte buffer (offsets
+        # 256-byte aligned), so that each step's input copy is one copy;
+        # returns the buffer and views of it shaped like `like`
+        offs, off = [], 0
+        for t in like:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(off, dtype=torch.uint8, device=device)
+        if pin:
+            buf = buf.pin_memory()
+        views = tuple(buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                      for o, t in zip(offs, like))
+        return buf, views
+
+    hpk = []
+    for L in layers:
+        buf, views = packed((L.d.q_idx, L.d.w_idx, L.d.q), "cpu", True)
+        for v, t in zip(views, (L.d.q_idx, L.d.w_idx, L.d.q)):
+            v.copy_(t.cpu())
+        hpk.append(buf)
+    dpk, dins = [], []
+    for L in layers:
+        sets = [packed((L.d.q_idx, L.d.w_idx, L.d.q), stream.device, False) for _ in range(2)]
+        dpk.append([b for b, _ in sets])
+        dins.append([v for _, v in sets])
     hout = [torch.empty(layers[0].out.shape, dtype=torch.float32).pin_memory() for _ in layers]
-    dins = [[(torch.empty_like(L.d.q_idx), torch.empty_like(L.d.w_idx), torch.empty_like(L.d.q))
-             for _ in range(2)] for L in layers]
     douts = [[torch.empty_like(L.out) for _ in range(2)] for L in layers]
     s_in = torch.cuda.Stream(device=stream.device)
     s_out = torch.cuda.Stream(device=stream.device)
@@ -298,8 +322,7 @@ def e2e_leg(layers, step, stream, steps, warmup, world, passes: int = 8):
             with torch.cuda.stream(s_in):
                 if i >= 2 * nl:
                     s_in.wait_event(dec[i - 2 * nl])   # the last decode that read this set
-                for dst, src in zip(dins[j][r], hin[j]):
-                    dst.copy_(src, non_blocking=True)
+                dpk[j][r].copy_(hpk[j], non_blocking=True)
                 h2d[i].record(s_in)
         for i in range(n):
             j, r = i % nl, (i // nl) % 2
@@ -339,16 +362,15 @@ def e2e_leg(layers, step, stream, steps, warmup, world, passes: int = 8):
     # the copies carried the right data: each layer's last host output equals,
     # bit for bit, what the device-timed steps left in its output
     same = all(torch.equal(hout[j], layers[j].out.cpu()) for j in range(nl))
-    hq_idx, hw_idx, hq = hin[0]
-    h2d_b = hq_idx.numel() * 2 + hw_idx.numel() * 4 + hq.numel() * 2
+    h2d_b = hpk[0].numel()   # the three inputs (and any alignment gap between them)
     return {"value": round(world * 1e3 / e2e_ms, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d_b), "d2h_bytes_per_step": int(hout[0].numel() * 4),
             "ms_per_step": round(e2e_ms, 5), "steps_timed": reps * n,
             "outputs_equal_device_path": bool(same),
             "launch": f"one CUDA graph of {n} steps ({passes} rounds of {nl} layers, two device "
-                      "sets of inputs and outputs per layer): input copies on one stream, "
-                      "csa_decode on another (one wait per round), each output copy on a third "
-                      "behind its decode"}
+                      "sets of inputs and outputs per layer): each step's inputs in one copy "
+                      "(packed q_idx, w_idx, q) on one stream, csa_decode on another (one wait "
+                      "per round), each output copy on a third behind its decode"}
 
 
 def ctx64k_leg(device, csa, stream, status, reps, seed):
