@@ -30,7 +30,7 @@
 // accumulates in TMEM across chunks.  Exponentials use the
 // running maximum of each head; when a chunk raises it by more than 8 (log2
 // units) the accumulated O^T and l are rescaled first, so a weight never
-// exceeds 2^8 and the two bf16 terms of P keep ~16 bits of it.
+// exceeds 2^8 and the two bf16 terms of P keep ~14 bits of it or more.
 //
 // Row slots of a token: its selected compressed rows (or, HCA, every visible
 // block) first, then its window rows starting at the next multiple of 4,
@@ -484,15 +484,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int w = 0; w < kLdWarps; ++w) msk |= static_cast<uint64_t>(S.maskw[st][w]) << (kLdRows * w);
             // lane l < 16 takes rows 0..31 of head hl, lane l + 16 rows 32..63
             float x[32];
-            float mc = -INFINITY;
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four short max chains
+            const bool full = msk == ~0ull;   // every row of the chunk valid: no mask per logit
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const uint32_t hi = __shfl_sync(0xffffffffu, sr[2 + (j >> 4)][j & 15], lane & 15);
                 const uint32_t v = upper ? hi : sr[j >> 4][j & 15];
                 const int row = (upper ? 32 : 0) + j;
-                x[j] = (msk >> row) & 1ull ? __uint_as_float(v) * A.scale_log2 : -INFINITY;
-                mc = fmaxf(mc, x[j]);
+                x[j] = (full || ((msk >> row) & 1ull)) ? __uint_as_float(v) * A.scale_log2 : -INFINITY;
+                mq[j & 3] = fmaxf(mq[j & 3], x[j]);
             }
+            float mc = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
             // a head whose maximum rises by more than kRescaleAbove rescales
             // what it has accumulated (every lane of the four warps takes part)
@@ -534,21 +536,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // P = 2^(x - m_ref) as hi + lo bf16 terms, this lane's half of row hl
             // (a head with no valid row yet keeps m_ref = -inf; its masked
-            // logits must give 0, not 2^(-inf + inf))
+            // logits must give 0, not 2^(-inf + inf)).  Both terms are the
+            // truncated upper halves of f32 values, so they cost integer
+            // operations only: hi = p with its low 16 bits cleared, lo = the
+            // same of p - hi; hi + lo is within 2^-14 of p (relative).
             const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-            float sum = 0.f;
+            float sq[2] = {0.f, 0.f};
             uint32_t phi[16], plo[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
                 const float p0 = fast_exp2(x[j] - mr);
                 const float p1 = fast_exp2(x[j + 1] - mr);
-                sum += p0 + p1;
-                const __nv_bfloat162 hi2 = __floats2bfloat162_rn(p0, p1);
-                const float2 hf = __bfloat1622float2(hi2);
-                const __nv_bfloat162 lo2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-                phi[j >> 1] = *reinterpret_cast<const uint32_t *>(&hi2);
-                plo[j >> 1] = *reinterpret_cast<const uint32_t *>(&lo2);
+                sq[(j >> 1) & 1] += p0 + p1;
+                const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                const float r0 = p0 - __uint_as_float(b0 & 0xFFFF0000u);
+                const float r1 = p1 - __uint_as_float(b1 & 0xFFFF0000u);
+                phi[j >> 1] = __byte_perm(b0, b1, 0x7632);
+                plo[j >> 1] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
             }
+            const float sum = sq[0] + sq[1];
             l += sum + __shfl_xor_sync(0xffffffffu, sum, 16);
             mbar_wait(&S.pfree[st], ph ^ 1u, A.status);   // PV of chunk i-2 is done with the buffer
             {
