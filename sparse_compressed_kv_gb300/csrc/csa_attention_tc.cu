@@ -9,14 +9,17 @@
 // gather buffer.  "PART A -- Next Session Clues", section 3: both kept where
 // they overlap.)
 //
-// A CTA owns one token, up to 64 heads and a contiguous range of the token's
-// row slots, which it walks in chunks of 64 rows.  Each row is read once for
-// all of the CTA's heads:
+// A CTA owns one token, up to 64 heads, a contiguous range of the token's
+// row slots, which it walks in chunks of 64 rows, and 1, 2 or all 4 of the
+// output's 128-column tiles (with few CTAs in the grid, 2 or 4 CTAs share a
+// row range: each computes its logits and weights in full and accumulates
+// only its own columns).  Each row is read from DRAM once for all heads:
 //   warp 1      TMEM allocator + tcgen05.mma issuer:
 //                 S  = Q . rows^T       M = 64 heads, N = 64 rows, K = 512
-//                 O^T += rows^T . P^T   M = 128 of the 512 columns (the row
-//                                       tile read MN-major), N = 64 heads,
-//                                       K = 64 rows; P as two bf16 terms
+//                 O^T += rows^T . P^T   M = 128 of the 512 columns per owned
+//                                       tile (the row tile read MN-major),
+//                                       N = 64 heads, K = 64 rows; P as two
+//                                       bf16 terms
 //   warps 0, 6+ fetch a chunk's rows by index into a two-stage ring (16-byte
 //               cp.async, 512 contiguous bytes per warp instruction, placed
 //               in the 128-byte-swizzled layout the MMA reads); a chunk is
@@ -34,8 +37,8 @@
 //
 // Row slots of a token: its selected compressed rows (or, HCA, every visible
 // block) first, then its window rows starting at the next multiple of 4,
-// padding masked.  With several splits per token
-// each CTA writes its partial (O, m, l) and a combine kernel merges them.
+// padding masked.  With several splits per token each CTA writes its
+// partial (O, m, l) of its columns and a combine kernel merges them.
 #include <math.h>
 
 #include "csa_device.cuh"
