@@ -651,6 +651,20 @@ def run_ours(args, rank, world, device):
         figraph = capture(findex_all, stream)
         fims = time_graphs([figraph], max(1, args.steps // len(layers)),
                            max(1, args.warmup // len(layers)), stream) / len(layers)
+        # the FP4 selection against the bf16 one on every layer (each exact on
+        # its own scores; the bf16 selection is the oracle's, see cpu_baseline)
+        rec, planted_kept = [], 0
+        for i, L in enumerate(layers):
+            ib = torch.empty_like(L.idx)
+            csa.csa_decode(L.layout, L.prm, L.d.q_idx, L.d.w_idx, L.d.k_idx, L.d.comp_kv, L.d.q,
+                           L.out, status, ws, idx_out=ib, stream=stream)
+            fstep(i, stream)
+            torch.cuda.synchronize()
+            sb = set(ib[0].cpu().tolist()) - {-1}
+            sf = set(L.idx[0].cpu().tolist()) - {-1}
+            rec.append(len(sb & sf) / max(1, len(sb)))
+            if L.wl.planted is not None:
+                planted_kept += int(all(int(b) in sf for b in L.wl.planted.tolist()))
         nv = ab["keys"] // (wl0.ihd * 2)
         fidx_bytes = nv * csa.FP4_ROW + (ab["indexer"] - ab["keys"])
         fstep_bytes = ab["step"] - ab["keys"] + nv * csa.FP4_ROW
@@ -661,7 +675,9 @@ def run_ours(args, rank, world, device):
             "indexer_bytes_per_launch": int(fidx_bytes),
             "indexer_hbm_frac": round(fidx_bytes / (fims * 1e-3) / 1e9 / hbm_peak, 4),
             "step_algorithmic_bytes": int(fstep_bytes),
-            "step_hbm_frac": round(fstep_bytes / (fms * 1e-3) / 1e9 / hbm_peak, 4)}
+            "step_hbm_frac": round(fstep_bytes / (fms * 1e-3) / 1e9 / hbm_peak, 4),
+            "recall_vs_bf16": {"min": round(min(rec), 6), "mean": round(statistics.mean(rec), 6),
+                               "layers": len(rec), "planted_all_selected_layers": planted_kept}}
         del fsingles, fgroup, figraph, frows
         check_status(status, "FP4")
 
