@@ -643,11 +643,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // splits without rows (m = -inf) skipped.  CTA = (head, token, column part)
 // of cw nsub threads and one more warp, cw = 128 / parts: thread (sub, c4)
 // holds columns 4 c4 .. 4 c4 + 3 of the part for splits sub, sub + nsub,
-// ..., loaded kCombPer at a time (all of them in flight), the last warp reads
+// ..., loaded kPer at a time (all of them in flight), the last warp reads
 // every split's (m, l) meanwhile, and the nsub partial sums meet in shared
 // memory in a fixed order.  Many splits: 4 parts of 128 columns (each CTA
 // reads a quarter of the partials); few: one part, fewer and larger CTAs.
-constexpr int kCombPer = 8;
 constexpr int kMaxSplits = 256;
 constexpr int kMlPer = kMaxSplits / 32;    // (m, l) pairs per lane of the last warp
 constexpr int kCombWideSub = 7;            // one part: at most 7 x 128 column threads
@@ -656,7 +655,10 @@ constexpr int kCombMaxThreads = 32 * kCombMaxSub + 32;
 constexpr int kCombRed = 960;              // partial sums of subs 1..: 30 x 32 or 6 x 128
 static_assert((kCombMaxSub - 1) * 32 <= kCombRed && (kCombWideSub - 1) * 128 <= kCombRed, "combine sums");
 
-template <int kCw>   // column threads per sub: 128 (one part) or 32 (four parts)
+// kCw: column threads per sub, 128 (one part) or 32 (four parts); kPer:
+// splits a thread loads per round, 8 or 4 (fewer registers: more CTAs per SM
+// when the grid is large, more subs in flight when splits are many).
+template <int kCw, int kPer>
 __global__ void __launch_bounds__(kCombMaxThreads) combine_tc_kernel(const TcParams A) {
     pdl_wait();
     pdl_launch_dependents();
@@ -673,15 +675,15 @@ __global__ void __launch_bounds__(kCombMaxThreads) combine_tc_kernel(const TcPar
     const int ns = A.splits;
     const float *mlb = A.part_ml + t * A.ml_t + h * 2;
     const int64_t mstride = A.ml_s;
-    // the first kCombPer of a thread's partial columns are in flight while
+    // the first kPer of a thread's partial columns are in flight while
     // the last warp reads (m, l) (every split writes its partial, zeros when
     // it has no rows, so the loads need not wait for the weights)
     const float *pb = A.part_o + t * A.po_t + h * kHD + col;
     const int64_t pstride = A.po_s;
-    float4 v[kCombPer];
+    float4 v[kPer];
     if (!ml_warp) {
 #pragma unroll
-        for (int k = 0; k < kCombPer; ++k) {
+        for (int k = 0; k < kPer; ++k) {
             const int sp = sub + k * nsub;
             if (sp < ns) v[k] = __ldcg(reinterpret_cast<const float4 *>(pb + sp * pstride));
         }
@@ -731,16 +733,16 @@ __global__ void __launch_bounds__(kCombMaxThreads) combine_tc_kernel(const TcPar
     }
     __syncthreads();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = sub; !ml_warp && base < ns; base += kCombPer * nsub) {
+    for (int base = sub; !ml_warp && base < ns; base += kPer * nsub) {
         if (base != sub) {
 #pragma unroll
-            for (int k = 0; k < kCombPer; ++k) {
+            for (int k = 0; k < kPer; ++k) {
                 const int sp = base + k * nsub;
                 if (sp < ns && wgt[sp] != 0.f) v[k] = __ldcg(reinterpret_cast<const float4 *>(pb + sp * pstride));
             }
         }
 #pragma unroll
-        for (int k = 0; k < kCombPer; ++k) {
+        for (int k = 0; k < kPer; ++k) {
             const int sp = base + k * nsub;
             if (sp < ns && wgt[sp] != 0.f) {
                 const float w = wgt[sp];
@@ -767,16 +769,21 @@ __global__ void __launch_bounds__(kCombMaxThreads) combine_tc_kernel(const TcPar
     }
 }
 
-// The combine's launch shape for ns splits: one part while 7 subs of 128
-// column threads hold every split in one round of loads, else four parts.
+// The combine's launch shape for ns splits of `heads` (head, token) pairs:
+// rounds of 4 loads when the grid is large or the splits many, else 8; one
+// part while 7 subs of 128 column threads hold every split in one round,
+// else four parts.
 struct CombShape {
     int parts, threads;
     void (*kernel)(const TcParams);
 };
-CombShape comb_shape(int ns) {
-    const int nsub = (ns + kCombPer - 1) / kCombPer;
-    if (nsub <= kCombWideSub) return {1, 128 * nsub + 32, combine_tc_kernel<128>};
-    return {4, 32 * (nsub < kCombMaxSub ? nsub : kCombMaxSub) + 32, combine_tc_kernel<32>};
+CombShape comb_shape(int ns, int64_t heads, int sm_count) {
+    const int nsub8 = (ns + 7) / 8, nsub4 = (ns + 3) / 4;
+    if (nsub8 > kCombWideSub)
+        return {4, 32 * (nsub4 < kCombMaxSub ? nsub4 : kCombMaxSub) + 32, combine_tc_kernel<32, 4>};
+    if (heads > 2 * static_cast<int64_t>(sm_count) && nsub4 <= kCombWideSub)
+        return {1, 128 * nsub4 + 32, combine_tc_kernel<128, 4>};
+    return {1, 128 * nsub8 + 32, combine_tc_kernel<128, 8>};
 }
 
 }  // namespace
@@ -827,7 +834,7 @@ cudaError_t launch_attention_tc(const Launch &lc, const RowSource &src, int32_t 
     A.ml_t = static_cast<int64_t>(plan.splits) * H * 2;
     A.ml_s = static_cast<int64_t>(H) * 2;
     A.raw_ml = raw_ml;
-    const CombShape cs = comb_shape(plan.splits);
+    const CombShape cs = comb_shape(plan.splits, static_cast<int64_t>(H) * T, lc.sm_count);
     e = set_kernel_smem(cs.kernel, 0);
     if (e != cudaSuccess) return e;
     return launch_pdl(cs.kernel, dim3(H, T, cs.parts), dim3(cs.threads), 0, lc.stream, A);
@@ -850,7 +857,7 @@ cudaError_t launch_partials_combine(const Launch &lc, int32_t P, int32_t T, int3
     A.po_s = static_cast<int64_t>(T) * H * kHD;
     A.ml_t = static_cast<int64_t>(H) * 2;
     A.ml_s = static_cast<int64_t>(T) * H * 2;
-    const CombShape cs = comb_shape(P);
+    const CombShape cs = comb_shape(P, static_cast<int64_t>(H) * T, lc.sm_count);
     cudaError_t e = set_kernel_smem(cs.kernel, 0);
     if (e != cudaSuccess) return e;
     return launch_pdl(cs.kernel, dim3(H, T, cs.parts), dim3(cs.threads), 0, lc.stream, A);
