@@ -40,8 +40,8 @@ UNIT = "tokens/s/layer"
 # committed ncu capture of that step (profiles/), and the SHA-256 prefix of the
 # kernel source it was taken on: once the source changes the figure no longer
 # describes the kernel, and the roofline reports traffic null.
-SELECT_TRAFFIC_BYTES = 67235072 + 107520
-SELECT_TRAFFIC_SOURCE = "eeff4dbf3442de38"
+SELECT_TRAFFIC_BYTES = 67232512 + 129792
+SELECT_TRAFFIC_SOURCE = "16e9667bff20d646"
 
 
 def select_traffic():

@@ -19,8 +19,8 @@
 // Folded selection.  The part of a token's range one CTA owns is a segment.
 // The epilogue keeps the segment's order-preserving score keys in shared
 // memory and histograms their top 11 bits.  When the segment ends it finds the
-// digit d where the count from the top reaches k' (about 1.25 x the segment's
-// share of top_k, plus a margin), writes every entry whose digit is >= d, in
+// digit d where the count from the top reaches k' (the segment's share of
+// top_k plus 16), writes every entry whose digit is >= d, in
 // block order, to the segment's candidate slot with the bound B = d << 21 (the
 // entries it left out all have keys below B), and adds those entries' digits
 // to the token's digit-1 histogram.  The last CTA to finish a segment of the
@@ -296,8 +296,10 @@ __device__ __forceinline__ void finalize_segment(const DecParams &P, DecSmem &S,
     int64_t len = s_end - s_begin;
     const bool lost = lo0 + len > kSegKeysMax;   // keys beyond the buffer (the host plan excludes it)
     if (lost) len = kSegKeysMax - lo0 > 0 ? kSegKeysMax - lo0 : 0;
-    // k': the segment's share of top_k with a margin
-    int64_t kq = (5 * static_cast<int64_t>(P.top_k) * len + 4 * nv - 1) / (4 * nv) + 16;
+    // k': the segment's share of top_k plus a margin of 16 (the digit's
+    // granularity, about a fifth of the score's magnitude, gives the proof
+    // its slack: with 1.25 x the share the largest bound was the same)
+    int64_t kq = (static_cast<int64_t>(P.top_k) * len + nv - 1) / nv + 16;
     kq = kq < P.top_k ? kq : P.top_k;
     kq = kq < len ? kq : len;
     const int hb = kD1Bins - PER * (gt + 1);
