@@ -486,19 +486,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int w = 0; w < kLdWarps; ++w) msk |= static_cast<uint64_t>(S.maskw[st][w]) << (kLdRows * w);
             // lane l < 16 takes rows 0..31 of head hl, lane l + 16 rows 32..63
+            // Every row valid and a scale >= 0: x keeps the raw logits, the
+            // maximum is taken on them (scaling by a constant >= 0 keeps the
+            // maximum, rounding included) and the scale enters the exponent
+            // pass as one fma.  Otherwise x holds the scaled logits (masked
+            // rows -inf) and the exponent pass multiplies by 1.
             float x[32];
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four short max chains
-            const bool full = msk == ~0ull;   // every row of the chunk valid: no mask per logit
+            float xs = 1.f;
+            if (msk == ~0ull && A.scale_log2 >= 0.f) {
+                xs = A.scale_log2;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const uint32_t hi = __shfl_sync(0xffffffffu, sr[2 + (j >> 4)][j & 15], lane & 15);
-                const uint32_t v = upper ? hi : sr[j >> 4][j & 15];
-                const int row = (upper ? 32 : 0) + j;
-                x[j] = (full || ((msk >> row) & 1ull)) ? __uint_as_float(v) * A.scale_log2 : -INFINITY;
-                mq[j & 3] = fmaxf(mq[j & 3], x[j]);
+                for (int j = 0; j < 32; ++j) {
+                    const uint32_t hi = __shfl_sync(0xffffffffu, sr[2 + (j >> 4)][j & 15], lane & 15);
+                    x[j] = __uint_as_float(upper ? hi : sr[j >> 4][j & 15]);
+                    mq[j & 3] = fmaxf(mq[j & 3], x[j]);
+                }
+            } else {
+                const uint32_t mh = static_cast<uint32_t>(msk >> (upper ? 32 : 0));
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const uint32_t hi = __shfl_sync(0xffffffffu, sr[2 + (j >> 4)][j & 15], lane & 15);
+                    const uint32_t v = upper ? hi : sr[j >> 4][j & 15];
+                    x[j] = ((mh >> j) & 1u) ? __uint_as_float(v) * A.scale_log2 : -INFINITY;
+                    mq[j & 3] = fmaxf(mq[j & 3], x[j]);
+                }
             }
             float mc = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-            mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
+            mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16)) * xs;
             // a head whose maximum rises by more than kRescaleAbove rescales
             // what it has accumulated (every lane of the four warps takes part)
             const bool need = hv && m_ref != -INFINITY && mc > m_ref + kRescaleAbove;
@@ -548,8 +563,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t phi[16], plo[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                const float p0 = fast_exp2(x[j] - mr);
-                const float p1 = fast_exp2(x[j + 1] - mr);
+                const float p0 = fast_exp2(fmaf(x[j], xs, -mr));
+                const float p1 = fast_exp2(fmaf(x[j + 1], xs, -mr));
                 sq[(j >> 1) & 1] += p0 + p1;
                 const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
                 const float r0 = p0 - __uint_as_float(b0 & 0xFFFF0000u);
