@@ -25,8 +25,10 @@
 //               in the 128-byte-swizzled layout the MMA reads); a chunk is
 //               handed to the MMA as soon as it has landed
 //   warps 2..5  online softmax: two lanes per head (the M = 64 accumulator's
-//               row h sits in lane h % 16 of lane quarter h / 16; its upper
-//               32 columns go to the lane 16 above), then the epilogue (one
+//               row h sits in lane h % 16 of lane quarter h / 16; one
+//               two-access tensor-memory load gives its lower 32 columns to
+//               that thread and its upper 32 to the thread 16 above), then
+//               the epilogue (one
 //               output column per lane).
 // S is double-buffered in TMEM and the MMA warp issues QK^T of chunk i+1
 // before PV of chunk i, so it runs during the softmax of chunk i; O^T
@@ -175,6 +177,18 @@ __device__ __forceinline__ void tmem_ld16_raw(uint32_t taddr, uint32_t (&r)[16])
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// 16 lanes x 16 columns twice: threads 0..15 read lanes 0..15 of the quarter
+// at columns c..c+15, threads 16..31 the same lanes at columns c+32..c+47
+__device__ __forceinline__ void tmem_ld16x2_raw(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 32;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
@@ -475,9 +489,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
             mbar_wait(&S.sfull[st], ph, A.status);
             tc_fence_after();
-            uint32_t sr[4][16];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) tmem_ld16_raw(tmem + lane_off + kSCol + st * kChunk + c4 * 16, sr[c4]);
+            // S of the M = 64 product sits in lanes 0..15 of the quarter: the
+            // two-access load gives lanes 0..15 columns c.. to threads 0..15
+            // and columns c + 32.. to threads 16..31
+            uint32_t sr[2][16];
+            tmem_ld16x2_raw(tmem + lane_off + kSCol + st * kChunk, sr[0]);
+            tmem_ld16x2_raw(tmem + lane_off + kSCol + st * kChunk + 16, sr[1]);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&S.sfree[st]);
@@ -498,16 +515,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 xs = A.scale_log2;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const uint32_t hi = __shfl_sync(0xffffffffu, sr[2 + (j >> 4)][j & 15], lane & 15);
-                    x[j] = __uint_as_float(upper ? hi : sr[j >> 4][j & 15]);
+                    x[j] = __uint_as_float(sr[j >> 4][j & 15]);
                     mq[j & 3] = fmaxf(mq[j & 3], x[j]);
                 }
             } else {
                 const uint32_t mh = static_cast<uint32_t>(msk >> (upper ? 32 : 0));
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const uint32_t hi = __shfl_sync(0xffffffffu, sr[2 + (j >> 4)][j & 15], lane & 15);
-                    const uint32_t v = upper ? hi : sr[j >> 4][j & 15];
+                    const uint32_t v = sr[j >> 4][j & 15];
                     x[j] = ((mh >> j) & 1u) ? __uint_as_float(v) * A.scale_log2 : -INFINITY;
                     mq[j & 3] = fmaxf(mq[j & 3], x[j]);
                 }
